@@ -1,0 +1,378 @@
+"""Benchmark of the sparse-attention forward stack on GB300.
+
+Default workload: the pages' 60M-model shape at training length, a 16-layer stack with
+B=8, H=8, N=1024, D=64, bf16 Q/K/V ~ N(0,1), W=12, Fibonacci base, staggered-linear alpha,
+mask (integer-distance) path.  One step = the forward of all 16 layers (16 launches,
+replayed from a CUDA graph), inputs resident in HBM.  Each layer has its own Q/K/V, so a
+step touches 537 MB > the 129 MB L2: no flush is needed between steps.
+
+Prints one JSON line (rank 0).  `--impl reference` times the float64 CPU oracle instead
+(on the host cores, on a bounded sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn fwd tokens/s and achieved HBM GB/s vs roofline, 1 GB300 (N=1024/4096)"
+UNIT = "tokens/s"
+HBM_FALLBACK_GBS = 6800.0
+
+WORKLOADS = {
+    # name: (B, H, N, L, W, base, schedule, mode, dtype, config id for the seeds)
+    "linear-stack-n1024": dict(B=8, H=8, N=1024, L=16, W=12, base="fib", sched="linear",
+                               mode="mask", dtype="bf16", cfg=1),
+    "coprime-fib-n4096": dict(B=2, H=8, N=4096, L=16, W=12, base="fib", sched="coprime",
+                              mode="mask", dtype="bf16", cfg=2),
+    "coprime-pow2-n4096": dict(B=2, H=8, N=4096, L=16, W=12, base="pow2", sched="coprime",
+                               mode="mask", dtype="bf16", cfg=12),
+    "learned-interp-n1024": dict(B=8, H=8, N=1024, L=16, W=10, base="fib", sched="learned",
+                                 mode="interp", dtype="bf16", cfg=3),
+    "long-mask-n131072": dict(B=1, H=8, N=131072, L=1, W=12, base="fib", sched="const1.5",
+                              mode="mask", dtype="bf16", cfg=4),
+    "long-interp-n131072": dict(B=1, H=8, N=131072, L=1, W=12, base="fib", sched="const1.5",
+                                mode="interp", dtype="bf16", cfg=4),
+}
+DEFAULT = "linear-stack-n1024"
+SECONDARY = ["coprime-fib-n4096", "coprime-pow2-n4096"]
+
+
+def alphas_for(w):
+    if w["sched"] == "linear":
+        from fibonacci_offset_sparse_gb300 import fib_attn as fa
+        return fa.fib_attn_schedule(fa.FIB_SCHED_LINEAR, w["L"])
+    if w["sched"] == "coprime":
+        from fibonacci_offset_sparse_gb300 import fib_attn as fa
+        return fa.fib_attn_schedule(fa.FIB_SCHED_COPRIME, w["L"], 7)
+    if w["sched"] == "learned":
+        from fibonacci_offset_sparse_gb300 import inputs
+        return list(inputs.learned_alpha(w["L"], w["cfg"]))
+    return [1.5] * w["L"]
+
+
+def compulsory_bytes(w):
+    elt = 2 if w["dtype"] == "bf16" else 4
+    return w["B"] * w["H"] * w["N"] * 64 * elt * 4  # Q, K, V read once + O written once
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for fn in ("common.cuh", "fwd.cu"):
+        with open(os.path.join(ROOT, "fibonacci_offset_sparse_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch of the forward kernel from the committed ncu summary of this
+    workload, or None when absent or taken on a different kernel source."""
+    p = os.path.join(ROOT, "profiles", f"fwd_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def setup(w, device):
+    import torch
+    from fibonacci_offset_sparse_gb300 import fib_attn as fa
+    from fibonacci_offset_sparse_gb300 import inputs
+    bk = fa.FIB_BASE_FIBONACCI if w["base"] == "fib" else fa.FIB_BASE_POW2
+    mode = fa.FIB_MODE_MASK if w["mode"] == "mask" else fa.FIB_MODE_INTERP
+    alphas = alphas_for(w)
+    plan = fa.fib_attn_plan_create(bk, alphas, w["W"], w["N"], mode)
+    host = [inputs.qkv(w["B"], w["H"], w["N"], 64, w["cfg"], l, w["dtype"]) for l in range(w["L"])]
+    dev = [tuple(t.to(device) for t in layer) for layer in host]
+    outs = [torch.empty_like(d[0]) for d in dev]
+    lses = [torch.empty(w["B"], w["H"], w["N"], dtype=torch.float32, device=device) for _ in dev]
+    adev = None
+    if w["mode"] == "interp":
+        adev = torch.tensor(alphas, dtype=torch.float32, device=device)
+    return plan, host, dev, outs, lses, adev
+
+
+def run_stack(fa, plan, dev, outs, lses, adev):
+    for l, (q, k, v) in enumerate(dev):
+        fa.fib_attn_fwd(plan, l, q, k, v, o=outs[l], lse=lses[l], alpha_dev=adev)
+
+
+def time_device(w, steps, warmup, device, rank, world):
+    import torch
+    from fibonacci_offset_sparse_gb300 import fib_attn as fa
+    plan, host, dev, outs, lses, adev = setup(w, device)
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        run_stack(fa, plan, dev, outs, lses, adev)  # first call outside capture
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        run_stack(fa, plan, dev, outs, lses, adev)
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index if device.index is not None else 0) as clk:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    res = dict(ms_total=ms, ms_per_step=ms / steps, launches=w["L"] * steps, clocks=clk.summary())
+    # end to end through the public API: pinned host inputs -> device -> 16 layers -> host O
+    pinned = [tuple(t.pin_memory() for t in layer) for layer in host]
+    o_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(t.numel() * t.element_size() for layer in pinned for t in layer)
+    d2h = sum(o.numel() * o.element_size() for o in o_host)
+    e2e_steps = max(1, min(steps, 5))
+
+    def e2e_step():
+        for l, (q, k, v) in enumerate(pinned):
+            dev[l][0].copy_(q, non_blocking=True)
+            dev[l][1].copy_(k, non_blocking=True)
+            dev[l][2].copy_(v, non_blocking=True)
+        run_stack(fa, plan, dev, outs, lses, adev)
+        for l in range(len(outs)):
+            o_host[l].copy_(outs[l], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms_e2e = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    res.update(ms_e2e_per_step=ms_e2e / e2e_steps, h2d=h2d, d2h=d2h, e2e_steps=e2e_steps,
+               e2e_launches=w["L"] * e2e_steps)
+    plan.close()
+    return res
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def time_oracle(w, n_layers_sample, rank_layers=None):
+    """Oracle seconds per layer of the workload on a sample of layers (and, for long
+    sequences, of heads); returns (seconds per full layer, sample description)."""
+    import numpy as np  # noqa: F401
+    import oracle
+    from fibonacci_offset_sparse_gb300 import inputs
+    alphas = alphas_for(w)
+    base = (lambda N: oracle.fibonacci_base()) if w["base"] == "fib" else oracle.pow2_base
+    heads = w["H"] if w["N"] <= 4096 else 1
+    layers = list(range(min(n_layers_sample, w["L"])))
+    t_total = 0.0
+    for l in layers:
+        q, k, v = inputs.qkv(w["B"], w["H"], w["N"], 64, w["cfg"], l, w["dtype"])
+        qf, kf, vf = (inputs.as_f64(x[:, :heads]) for x in (q, k, v))
+        t0 = time.perf_counter()
+        oracle.attend(qf, kf, vf, alphas[l], base(w["N"]), w["W"], w["mode"])
+        t_total += time.perf_counter() - t0
+    frac_heads = heads / w["H"]
+    per_layer = t_total / len(layers) / frac_heads
+    desc = (f"oracle forward on {len(layers)} of {w['L']} layers" +
+            (f", {heads} of {w['H']} heads" if heads < w["H"] else "") + ", float64 numpy, 1 thread")
+    return per_layer, desc
+
+
+def oracle_tokens_per_s(w, per_layer_s):
+    return w["B"] * w["N"] / (per_layer_s * w["L"])
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    w = WORKLOADS[args.workload]
+    cfg = {"workload": args.workload, "B": w["B"], "H": w["H"], "N": w["N"], "D": 64, "layers": w["L"],
+           "W": w["W"], "base": {"fib": "fibonacci 1..987", "pow2": "powers of two < N"}[w["base"]],
+           "schedule": w["sched"], "path": w["mode"] + " forward",
+           "l2": "no flush: each step reads every layer's own Q/K/V (inputs > L2 per step)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        per_layer, desc = time_oracle(w, 1)  # warm/size
+        vals = []
+        for _ in range(args.warmup):
+            pass
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            pl, desc = time_oracle(w, 1)
+            vals.append(pl)
+        el = time.perf_counter() - t0
+        per_layer = statistics.mean(vals)
+        v = oracle_tokens_per_s(w, per_layer)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_layer * w["L"] * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic N(0,1), seeded", "config": cfg,
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                 "sample": desc + f"; each step is one layer, scaled to the {w['L']}-layer stack",
+                                 "host_cores_available": len(os.sched_getaffinity(0))},
+                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "wall_s": el}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from fibonacci_offset_sparse_gb300 import fib_attn as fa
+    fa.lib()  # fails loudly when the library is not built
+
+    r = time_device(w, args.steps, args.warmup, device, rank, world)
+    tokens_step = w["B"] * w["N"]
+    value = tokens_step * world / (r["ms_per_step"] / 1e3)
+    e2e_value = tokens_step * world / (r["ms_e2e_per_step"] / 1e3)
+    peak, peak_kind = read_peaks()
+    launch_s = r["ms_per_step"] / 1e3 / w["L"]
+    algo = compulsory_bytes(w)
+    achieved = algo / launch_s / 1e9
+    traffic = ncu_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"],
+        "data": "synthetic: i.i.d. N(0,1) Q/K/V per layer (seeded), shaped like the pages' 60M model",
+        "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_kind": peak_kind + (" (hbm_gbs, burst copy)" if peak_kind == "measured" else ""),
+                     "algorithmic_bytes_per_launch": algo,
+                     "avg_launch_us": launch_s * 1e6},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"]},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if not args.no_secondary and args.workload == DEFAULT:
+        sec = {}
+        for name in SECONDARY:
+            ws = WORKLOADS[name]
+            rs = time_device(ws, args.steps, args.warmup, device, rank, world)
+            ls = rs["ms_per_step"] / 1e3 / ws["L"]
+            ach = compulsory_bytes(ws) / ls / 1e9
+            sec[name] = {"value": ws["B"] * ws["N"] * world / (rs["ms_per_step"] / 1e3), "unit": UNIT,
+                         "ms_per_step": rs["ms_per_step"], "avg_launch_us": ls * 1e6,
+                         "achieved_gbs": ach, "frac": ach / peak, "traffic": ncu_traffic(name)}
+            line["gpu_launches"] += rs["launches"] + rs["e2e_launches"]
+        line["secondary"] = sec
+    line["gpu_launches"] += r["e2e_launches"]
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        per_layer, desc = time_oracle(w, 3)
+        line["cpu_baseline"] = {"value": oracle_tokens_per_s(w, per_layer), "unit": UNIT, "cores": 1,
+                                "kind": "oracle", "sample": desc + ", scaled to the full stack",
+                                "host_cores_available": len(os.sched_getaffinity(0))}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,168 @@
+/*
+ * fib_attn.h -- C ABI of the GB300 (sm_103a) Depth-Staggered Fibonacci Spacing sparse
+ * attention library (libfibattn.so).
+ *
+ * The operation ("Depth-Staggered Fibonacci Spacing for Sparse Attention: Static
+ * Schedules Beat Learned Dilation and Extrapolate Where Dense Attention Fails",
+ * Methodology > "Attended set", "Scaling", "Implementation"):
+ *   each causal query i of a layer attends to a dense local window of W keys
+ *   (distances 0..W-1, the query itself included) plus sparse keys at distances
+ *   d_k = alpha_l * f_k, f the Fibonacci list 1, 2, 3, 5, ..., 987 (or the power-of-two
+ *   control base), alpha_l one scalar per layer in [0.5, 1.5].  RoPE is applied to Q and
+ *   K before the gather.  Integer distances take the boolean-mask path (MASK); non-integer
+ *   ones are served by linear interpolation between the two bracketing K/V rows, which
+ *   gives alpha a gradient (INTERP).
+ *
+ * Readings where the pages are silent:
+ *   - a static non-integer distance is rounded half-to-even (binary64 product alpha*f);
+ *     MASK keeps the distinct distances d >= W, INTERP keeps rungs with d > W-1;
+ *   - a rung is attended by query i iff d <= i (no padding, no clamping);
+ *   - softmax scale 1/sqrt(D); RoPE rotate-half pairs (m, m+D/2), positions 0..N-1,
+ *     angle p * rope_base^(-2m/D); V is not rotated;
+ *   - INTERP blends the rotated rows: k~ = (1-w) k'[i-lo] + w k'[i-lo-1], lo = floor(d),
+ *     w = d - lo; dalpha is the right derivative (lo held fixed, dw/dalpha = f), the
+ *     term is zero where row i-lo-1 does not exist.
+ *
+ * Conventions for every entry point:
+ *   - Return value: a fib_status code; no function aborts, prints or exits.
+ *   - Tensors are caller-owned device buffers, contiguous [B, H, N, D] row-major with
+ *     D = 64, 16-byte aligned.  Q/K/V/O/dO/dQ/dK/dV share one dtype (fib_dtype); LSE
+ *     ([B, H, N]) and dalpha are float32.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device entry points
+ *     only enqueue work on it and never synchronise, except fib_attn_last_device_status.
+ *   - The library owns only the plan (host struct + its small device RoPE tables and
+ *     status word, allocated by fib_attn_plan_create on the device current at that time;
+ *     every device call must run with that same device current).
+ *   - There is no CPU fallback: without a CUDA device the device entry points return
+ *     FIB_ERR_CUDA.
+ */
+#ifndef FIB_ATTN_H
+#define FIB_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct fib_attn_plan_s* fib_attn_plan_t;
+
+enum fib_status {
+  FIB_OK = 0,
+  FIB_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, out-of-range index   */
+  FIB_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (D != 64)  */
+  FIB_ERR_CUDA = 3,          /* a CUDA runtime call failed (incl. no device)            */
+  FIB_ERR_NOMEM = 4,         /* host or device allocation failed                        */
+  FIB_ERR_TIMEOUT = 5,       /* a bounded device wait gave up (see last_device_status)  */
+  FIB_ERR_DEVICE_ASSERT = 6  /* a device-side check recorded a violated invariant       */
+};
+
+enum fib_base_kind { FIB_BASE_FIBONACCI = 0, FIB_BASE_POW2 = 1, FIB_BASE_CUSTOM = 2 };
+enum fib_schedule_kind { FIB_SCHED_FIXED = 0, FIB_SCHED_LINEAR = 1, FIB_SCHED_COPRIME = 2 };
+enum fib_mode { FIB_MODE_MASK = 0, FIB_MODE_INTERP = 1 };
+enum fib_dtype { FIB_DTYPE_F32 = 0, FIB_DTYPE_BF16 = 1 };
+
+#define FIB_HEAD_DIM 64   /* the only head dimension built */
+#define FIB_MAX_RUNGS 32  /* rungs per layer, after dedup */
+#define FIB_MAX_WINDOW 64 /* largest window W */
+#define FIB_MAX_LAYERS 256
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* fib_attn_error_string(int code);
+
+/* ---------------------------------------------------------------- host-only planner --
+ * These run on the CPU only and need no GPU.                                           */
+
+/* Base list f ("Attended set" / "Controls").  FIBONACCI: 1, 2, 3, 5, ..., 987 (15
+ * entries, the repeated leading 1 dropped).  POW2: {2^k : 2^k < N} (reach-matched
+ * control; N >= 2).  Writes min(count, cap) entries to out, the full count to *n_out.
+ * FIB_ERR_INVALID_ARG on a bad kind, N < 2 for POW2, cap < 0 or null n_out.            */
+int fib_attn_base(int base_kind, int N, int32_t* out, int cap, int* n_out);
+
+/* Per-layer alpha ("Experimental variables").  FIXED: 1.  LINEAR: 0.5 + l/(L-1) in
+ * binary64 (0.5 at layer 0, 1.5 at the last; L >= 2).  COPRIME: alpha_lin[(stride*l)
+ * mod L] with gcd(stride, L) = 1 (the pages use stride 7, L = 16).  alpha_out holds
+ * n_layers doubles.  FIB_ERR_INVALID_ARG on bad kind, L out of [1, FIB_MAX_LAYERS],
+ * L < 2 for a ramp, or a stride not coprime with L.                                   */
+int fib_attn_schedule(int kind, int n_layers, int stride, double* alpha_out);
+
+/* MASK-path distances of one layer ("Scaling": d_k = alpha f_k): the sorted distinct
+ * values round_half_even(alpha * f) with W <= d <= N-1.  Writes min(count, cap) to out,
+ * count to *n_out.  FIB_ERR_INVALID_ARG on null pointers, n_base < 0, W < 1, N < 1,
+ * alpha not finite or <= 0.                                                           */
+int fib_attn_mask_distances(const int32_t* base, int n_base, double alpha, int W, int N,
+                            int32_t* out, int cap, int* n_out);
+
+/* INTERP-path rungs of one layer ("Implementation": linear interpolation between the
+ * bracketing rows): for each distinct f (ascending) with d = alpha*f, W-1 < d <= N-1:
+ * f, lo = floor(d), w = (float)(d - lo).  Same size/error rules as above.               */
+int fib_attn_interp_rungs(const int32_t* base, int n_base, double alpha, int W, int N,
+                          int32_t* f_out, int32_t* lo_out, float* w_out, int cap,
+                          int* n_out);
+
+/* ------------------------------------------------------------------------- plan ----
+ * A plan fixes (base, per-layer alpha, W, N_max, D, mode, RoPE base) for a layer stack
+ * and uploads the RoPE tables (built in binary64 on the host, stored float32) for
+ * positions < N_max to the current device.  base_kind CUSTOM reads custom_base[n_custom]
+ * (positive integers); otherwise custom_base is ignored.  alpha[n_layers] is copied.
+ * Constraints: 1 <= W <= FIB_MAX_WINDOW, 1 <= N_max <= 1<<20, D == 64
+ * (else FIB_ERR_UNSUPPORTED), every alpha finite and > 0, rope_base > 1.
+ * Errors: FIB_ERR_INVALID_ARG, FIB_ERR_UNSUPPORTED, FIB_ERR_NOMEM, FIB_ERR_CUDA.        */
+int fib_attn_plan_create(fib_attn_plan_t* out, int base_kind, const int32_t* custom_base,
+                         int n_custom, const double* alpha, int n_layers, int W, int N_max,
+                         int D, int mode, double rope_base);
+
+/* Frees the plan and its device tables (synchronises the device first).  NULL is OK. */
+int fib_attn_plan_destroy(fib_attn_plan_t p);
+
+/* Host copy of the MASK distances (mode MASK) or INTERP lo values (mode INTERP) that the
+ * plan uses for `layer` at sequence length N (N <= N_max).                             */
+int fib_attn_plan_distances(fib_attn_plan_t p, int layer, int N, int32_t* out, int cap,
+                            int* n_out);
+
+/* ---------------------------------------------------------------------- forward ----
+ * O = attention output (dtype of the inputs), lse = natural-log sum of exp(scores),
+ * both for layer `layer` of the plan at sequence length N (1 <= N <= N_max).
+ * q, k, v, o: [B, H, N, 64] device, dtype `dtype`.  lse: [B, H, N] float32 device, or
+ * NULL to skip writing it.  alpha_dev (INTERP only): device float32 alpha[n_layers]
+ * (a learned parameter; element `layer` is used, exactly as a float32) or NULL to use
+ * the plan's binary64 alpha.  MASK ignores alpha_dev.  O must not alias q, k or v.
+ * Errors: FIB_ERR_INVALID_ARG (null/misaligned pointers, sizes, layer), FIB_ERR_CUDA.  */
+int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
+                 const void* q, const void* k, const void* v, void* o, float* lse,
+                 const float* alpha_dev, void* stream);
+
+/* --------------------------------------------------------------------- backward ----
+ * Gradients of l = sum(O * dO) for one layer, given the forward's o and lse.
+ * dq, dk, dv: [B, H, N, 64] device (dtype of the inputs), fully written.
+ * dalpha: device float32 scalar, written (not accumulated) with dl/dalpha_layer in
+ * INTERP mode and 0 in MASK mode (static distances carry no alpha gradient).
+ * workspace: device scratch of at least fib_attn_bwd_workspace_size(p, B, H, N) bytes,
+ * 256-byte aligned, caller-owned; its contents on entry are ignored.
+ * Errors as fib_attn_fwd, plus FIB_ERR_INVALID_ARG for a short/misaligned workspace.  */
+size_t fib_attn_bwd_workspace_size(fib_attn_plan_t p, int B, int H, int N);
+int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
+                 const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                 float* dalpha, const float* alpha_dev, void* workspace, size_t ws_bytes,
+                 void* stream);
+
+/* ---------------------------------------------------------------- debug / status ----
+ * The attended index sets of queries [i_begin, i_end), produced by the same device
+ * index code as the forward kernel.  out_dev: int32 [(i_end-i_begin), W + FIB_MAX_RUNGS]
+ * device; slot s < W holds the window row i-s, slot W+r holds rung r's row (MASK: i-d;
+ * INTERP: i-lo, whose partner row i-lo-1 carries weight w), -1 where not attended.
+ * w_out_dev: float32 [FIB_MAX_RUNGS] device (INTERP weights; 0 for MASK) or NULL.      */
+int fib_attn_debug_indices(fib_attn_plan_t p, int layer, int N, int i_begin, int i_end,
+                           int32_t* out_dev, float* w_out_dev, const float* alpha_dev,
+                           void* stream);
+
+/* Synchronises the plan's device, then returns and clears the device status word:
+ * FIB_OK, FIB_ERR_TIMEOUT (a bounded wait gave up) or FIB_ERR_DEVICE_ASSERT.          */
+int fib_attn_last_device_status(fib_attn_plan_t p);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FIB_ATTN_H */

@@ -1,0 +1,282 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on seeded inputs.
+
+Tolerances:
+  * index sets: bit-exact;
+  * O: max-abs <= 1e-5 for float32 inputs; <= 1e-2 for bf16 inputs (float32 accumulation)
+    against the oracle run on the same bf16-rounded values, plus the bf16 output's own
+    rounding (at most half an ulp, bounded by 2^-8 |O|);
+  * LSE (float32 output): 1e-5 (float32 inputs), 1e-3 (bf16 inputs);
+  * dQ, dK, dV, dalpha: relative L2 <= 2e-2.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fibonacci_offset_sparse_gb300 import fib_attn as fa
+from fibonacci_offset_sparse_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+F32_ATOL = 1e-5
+BF16_ATOL = 1e-2
+REL_L2 = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from fibonacci_offset_sparse_gb300 import build as b
+    import os
+    if not os.path.exists(b.LIB):
+        b.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return fa.lib()
+
+
+def _base_fn(kind):
+    if kind == "fib":
+        return lambda N: oracle.fibonacci_base()
+    if kind == "pow2":
+        return oracle.pow2_base
+    return lambda N: list(kind)
+
+
+def _plan(kind, alphas, W, N_max, mode):
+    bk = {"fib": fa.FIB_BASE_FIBONACCI, "pow2": fa.FIB_BASE_POW2}.get(kind, fa.FIB_BASE_CUSTOM)
+    custom = None if bk != fa.FIB_BASE_CUSTOM else list(kind)
+    m = fa.FIB_MODE_MASK if mode == "mask" else fa.FIB_MODE_INTERP
+    return fa.fib_attn_plan_create(bk, alphas, W, N_max, m, custom_base=custom)
+
+
+def _check_o(o_gpu, O_ref, dtype, what=""):
+    og = o_gpu.detach().double().cpu().numpy()
+    err = np.abs(og - O_ref)
+    if dtype == "f32":
+        assert err.max() <= F32_ATOL, f"{what} max-abs {err.max():.3e}"
+    else:
+        bound = BF16_ATOL + np.abs(O_ref) * 2.0 ** -8
+        assert np.all(err <= bound), f"{what} max-abs {err.max():.3e} (worst excess {(err - bound).max():.3e})"
+    return err.max()
+
+
+def _check_lse(lse_gpu, lse_ref, dtype, what=""):
+    lg = lse_gpu.detach().double().cpu().numpy()
+    tol = 1e-5 if dtype == "f32" else 1e-3
+    err = np.abs(lg - lse_ref).max()
+    assert err <= tol, f"{what} lse max-abs {err:.3e}"
+
+
+def _rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def _run_fwd(kind, alphas, W, B, H, N, dtype, mode, layers, config, alpha_dev=None, heads=None):
+    plan = _plan(kind, alphas, W, N, mode)
+    adev = None if alpha_dev is None else torch.tensor(alpha_dev, dtype=torch.float32, device="cuda")
+    for layer in layers:
+        q, k, v = inputs.qkv(B, H, N, 64, config, layer, dtype)
+        o, lse = fa.fib_attn_fwd(plan, layer, q.cuda(), k.cuda(), v.cuda(), alpha_dev=adev)
+        torch.cuda.synchronize()
+        a = alphas[layer] if alpha_dev is None else float(np.float32(alpha_dev[layer]))
+        hs = slice(None) if heads is None else heads
+        O_ref, lse_ref = oracle.attend(inputs.as_f64(q[:, hs]), inputs.as_f64(k[:, hs]),
+                                       inputs.as_f64(v[:, hs]), a, _base_fn(kind)(N), W, mode)
+        _check_o(o[:, hs], O_ref, dtype, f"layer {layer}")
+        _check_lse(lse[:, hs], lse_ref, dtype, f"layer {layer}")
+    plan.close()
+
+
+# ------------------------------------------------------------------ the five workloads
+def test_c0_fp32_mask_alpha1():
+    """1 layer, B=1, H=1, N=256, fp32, W=8, Fibonacci, alpha=1 (mask path)."""
+    _run_fwd("fib", [1.0], 8, 1, 1, 256, "f32", "mask", [0], 0)
+    # the interpolated path at alpha = 1 reduces to the mask path
+    _run_fwd("fib", [1.0], 8, 1, 1, 256, "f32", "interp", [0], 0)
+
+
+def test_c1_linear_stack_bf16():
+    """16 layers, B=8, H=8, N=1024, bf16, W=12, Fibonacci, linear schedule, mask path."""
+    _run_fwd("fib", oracle.schedule("linear", 16), 12, 8, 8, 1024, "bf16", "mask", range(16), 1)
+
+
+@pytest.mark.parametrize("kind", ["fib", "pow2"])
+def test_c2_coprime_extrapolation_bf16(kind):
+    """16 layers, B=2, H=8, N=4096, bf16, W=12, coprime schedule; layers sampled."""
+    _run_fwd(kind, oracle.schedule("coprime", 16), 12, 2, 8, 4096, "bf16", "mask",
+             [0, 7, 9, 15], 2 if kind == "fib" else 12)
+
+
+@pytest.mark.parametrize("mode", ["mask", "interp"])
+def test_c4_long_context_bf16(mode):
+    """1 layer, B=1, H=8, N=131072, bf16, W=12, alpha=1.5; oracle on two heads."""
+    _run_fwd("fib", [1.5], 12, 1, 8, 131072, "bf16", mode, [0], 4, heads=slice(2, 4))
+
+
+def test_c3_learned_fwd_bwd_bf16():
+    """16 layers, B=8, H=8, N=1024, bf16, W=10, alpha ~ U[0.9, 1.1] (device float32),
+    interp forward + backward; layers sampled."""
+    L, B, H, N, W = 16, 8, 8, 1024, 10
+    alpha = inputs.learned_alpha(L, 3)
+    plan = _plan("fib", [1.0] * L, W, N, "interp")
+    adev = torch.tensor(alpha, dtype=torch.float32, device="cuda")
+    for layer in (0, 5, 11):
+        q, k, v = inputs.qkv(B, H, N, 64, 3, layer, "bf16")
+        dO = inputs.upstream_grad(B, H, N, 64, 3, layer, "bf16")
+        qc, kc, vc, dOc = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+        o, lse = fa.fib_attn_fwd(plan, layer, qc, kc, vc, alpha_dev=adev)
+        dq, dk, dv, da = fa.fib_attn_bwd(plan, layer, qc, kc, vc, o, lse, dOc, alpha_dev=adev)
+        torch.cuda.synchronize()
+        a = float(alpha[layer])
+        qf, kf, vf, gf = (inputs.as_f64(x) for x in (q, k, v, dO))
+        O_ref, lse_ref = oracle.attend(qf, kf, vf, a, oracle.fibonacci_base(), W, "interp")
+        _check_o(o, O_ref, "bf16", f"layer {layer}")
+        _check_lse(lse, lse_ref, "bf16")
+        # the backward consumes the kernel's bf16 O; the oracle differentiates its own forward
+        rq, rk, rv, ra = oracle.attend_bwd(qf, kf, vf, gf, a, oracle.fibonacci_base(), W, "interp")
+        for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+            e = _rel_l2(g.double().cpu().numpy(), r)
+            assert e <= REL_L2, f"layer {layer} {name} rel-L2 {e:.3e}"
+        e = abs(float(da.item()) - ra) / max(abs(ra), 1e-30)
+        assert e <= REL_L2, f"layer {layer} dalpha {da.item()} vs {ra} rel {e:.3e}"
+    plan.close()
+
+
+# ------------------------------------------------------------------ index sets (bit-exact)
+def _check_indices(kind, alphas, W, N, mode, layers, alpha_dev=None, ranges=None):
+    plan = _plan(kind, alphas, W, N, mode)
+    adev = None if alpha_dev is None else torch.tensor(alpha_dev, dtype=torch.float32, device="cuda")
+    for layer in layers:
+        a = alphas[layer] if alpha_dev is None else float(np.float32(alpha_dev[layer]))
+        ref = oracle.index_sets(_base_fn(kind)(N), a, W, N, mode)
+        for (i0, i1) in (ranges or [(0, N)]):
+            rows, w = fa.fib_attn_debug_indices(plan, layer, N, i0, i1, alpha_dev=adev)
+            rows = rows.cpu().numpy()
+            w = w.cpu().numpy()
+            keys = oracle.virtual_keys(_base_fn(kind)(N), a, W, N, mode)
+            nr = len(keys) - W
+            for (_, _, wk, _), wg in zip(keys[W:], w[:nr]):
+                assert wg == np.float32(wk)
+            for i in range(i0, i1):
+                got = [(int(x), float(w[s - W]) if s >= W else 0.0)
+                       for s, x in enumerate(rows[i - i0]) if x >= 0]
+                want = [(r, float(np.float32(ww))) for (r, ww) in ref[i]]
+                assert got == want, (layer, i)
+    plan.close()
+
+
+def test_indices_c0_and_c1():
+    _check_indices("fib", [1.0], 8, 256, "mask", [0])
+    _check_indices("fib", oracle.schedule("linear", 16), 12, 1024, "mask", range(16))
+
+
+@pytest.mark.parametrize("kind", ["fib", "pow2"])
+def test_indices_c2(kind):
+    _check_indices(kind, oracle.schedule("coprime", 16), 12, 4096, "mask", range(16),
+                   ranges=[(0, 40), (1000, 1100), (4000, 4096)])
+
+
+def test_indices_c3_device_alpha_and_c4():
+    a = inputs.learned_alpha(16, 3)
+    _check_indices("fib", [1.0] * 16, 10, 1024, "interp", range(16), alpha_dev=a)
+    for mode in ("mask", "interp"):
+        _check_indices("fib", [1.5], 12, 131072, mode, [0],
+                       ranges=[(0, 64), (1470, 1500), (131000, 131072)])
+
+
+# ------------------------------------------------------------------ edge cases, fp32
+@pytest.mark.parametrize("mode", ["mask", "interp"])
+@pytest.mark.parametrize("N,W,alpha,kind", [
+    (1, 12, 1.0, "fib"),            # a single query
+    (7, 12, 1.3, "fib"),            # N < W
+    (65, 8, 0.5, "fib"),            # one full tile + a ragged tail of 1
+    (200, 1, 1.5, "fib"),           # window of one (self only)
+    (300, 64, 1.2345, "fib"),       # largest window
+    (257, 6, 0.77, "pow2"),         # power-of-two base
+    (150, 4, 1.0, (37,)),           # single-rung custom base
+    (129, 12, 0.5 + 9 / 15, "fib"),  # alpha = binary64 1.1 (rounding canary)
+])
+def test_edge_cases_fp32(mode, N, W, alpha, kind):
+    B, H = 2, 3
+    plan = _plan(kind, [alpha], W, N, mode)
+    q, k, v = inputs.qkv(B, H, N, 64, 100 + N, W, "f32")
+    o, lse = fa.fib_attn_fwd(plan, 0, q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    O_ref, lse_ref = oracle.attend(inputs.as_f64(q), inputs.as_f64(k), inputs.as_f64(v), alpha,
+                                   _base_fn(kind)(N), W, mode)
+    _check_o(o, O_ref, "f32")
+    _check_lse(lse, lse_ref, "f32")
+    plan.close()
+
+
+@pytest.mark.parametrize("mode,alpha", [("interp", 1.2345), ("interp", 0.6789), ("interp", 1.0),
+                                        ("mask", 0.5 + 4 / 15)])
+@pytest.mark.parametrize("device_alpha", [False, True])
+def test_backward_fp32(mode, alpha, device_alpha):
+    B, H, N, W = 2, 2, 333, 8
+    if device_alpha:
+        alpha = float(np.float32(alpha))
+    plan = _plan("fib", [alpha], W, N, mode)
+    q, k, v = inputs.qkv(B, H, N, 64, 200, 0, "f32")
+    dO = inputs.upstream_grad(B, H, N, 64, 200, 0, "f32")
+    adev = torch.tensor([alpha], dtype=torch.float32, device="cuda") if device_alpha else None
+    qc, kc, vc, dOc = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+    o, lse = fa.fib_attn_fwd(plan, 0, qc, kc, vc, alpha_dev=adev)
+    dq, dk, dv, da = fa.fib_attn_bwd(plan, 0, qc, kc, vc, o, lse, dOc, alpha_dev=adev)
+    torch.cuda.synchronize()
+    qf, kf, vf, gf = (inputs.as_f64(x) for x in (q, k, v, dO))
+    rq, rk, rv, ra = oracle.attend_bwd(qf, kf, vf, gf, alpha, oracle.fibonacci_base(), W, mode)
+    for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        e = _rel_l2(g.double().cpu().numpy(), r)
+        assert e <= 1e-5, f"{name} rel-L2 {e:.3e}"
+    if mode == "mask":
+        assert float(da.item()) == 0.0
+    else:
+        assert abs(float(da.item()) - ra) <= 1e-4 * abs(ra) + 1e-4, (float(da.item()), ra)
+    # deterministic: a second run gives identical bits
+    dq2, dk2, dv2, da2 = fa.fib_attn_bwd(plan, 0, qc, kc, vc, o, lse, dOc, alpha_dev=adev)
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2) and torch.equal(da, da2)
+    plan.close()
+
+
+# ------------------------------------------------------------------ error paths on a GPU
+def test_device_error_paths():
+    plan = _plan("fib", [1.0, 1.0], 12, 256, "mask")
+    lib = fa.lib()
+    B, H, N = 1, 2, 128
+    q = torch.zeros(B, H, N, 64, device="cuda")
+    o = torch.empty_like(q)
+    s = torch.cuda.current_stream().cuda_stream
+
+    def fwd(layer=0, n=N, dtype=0, qp=None, op=None, lsep=None):
+        return lib.fib_attn_fwd(plan.handle, layer, B, H, n, dtype, qp or q.data_ptr(), q.data_ptr(),
+                                q.data_ptr(), op or o.data_ptr(), lsep, None, s)
+
+    assert fwd() == fa.FIB_OK
+    assert fwd(layer=2) == fa.FIB_ERR_INVALID_ARG            # layer out of range
+    assert fwd(layer=-1) == fa.FIB_ERR_INVALID_ARG
+    assert fwd(n=257) == fa.FIB_ERR_INVALID_ARG              # N > N_max
+    assert fwd(n=0) == fa.FIB_ERR_INVALID_ARG
+    assert fwd(dtype=5) == fa.FIB_ERR_INVALID_ARG
+    assert fwd(qp=q.data_ptr() + 4) == fa.FIB_ERR_INVALID_ARG   # misaligned
+    assert fwd(op=q.data_ptr()) == fa.FIB_ERR_INVALID_ARG       # o aliases q
+    assert fwd(lsep=q.data_ptr() + 2) == fa.FIB_ERR_INVALID_ARG
+    ws_need = fa.fib_attn_bwd_workspace_size(plan, B, H, N)
+    ws = torch.empty(ws_need, dtype=torch.uint8, device="cuda")
+    lse = torch.empty(B, H, N, device="cuda")
+    g = [torch.empty_like(q) for _ in range(3)]
+    da = torch.empty(1, device="cuda")
+    args = [plan.handle, 0, B, H, N, 0, q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(),
+            lse.data_ptr(), q.data_ptr(), g[0].data_ptr(), g[1].data_ptr(), g[2].data_ptr(),
+            da.data_ptr(), None, ws.data_ptr()]
+    assert lib.fib_attn_bwd(*args, ws_need - 1, s) == fa.FIB_ERR_INVALID_ARG   # short workspace
+    bad = list(args)
+    bad[-1] = ws.data_ptr() + 16
+    assert lib.fib_attn_bwd(*bad, ws_need, s) == fa.FIB_ERR_INVALID_ARG        # misaligned ws
+    assert lib.fib_attn_bwd(*args, ws_need, s) == fa.FIB_OK
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    plan.close()
