@@ -19,6 +19,11 @@ namespace fibattn {
 cudaError_t launch_fwd(const LayerTable& t, int B, int H, int N, int dtype, const void* q,
                        const void* k, const void* v, void* o, float* lse, const float2* lo_tab,
                        const float2* hi_tab, cudaStream_t stream);
+bool tc_supported(const LayerTable& t);
+cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k,
+                          const void* v, void* o, float* lse, const float2* lo_tab,
+                          const float2* hi_tab, int* status, unsigned long long wait_ns,
+                          int skip_first_rung_copy, cudaStream_t stream);
 cudaError_t launch_debug_indices(const LayerTable& t, int N, int i0, int i1, int32_t* out,
                                  float* w_out, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int H, int N);
@@ -40,6 +45,8 @@ struct fib_attn_plan_s {
   float2* d_lo = nullptr;
   float2* d_hi = nullptr;
   int* d_status = nullptr;
+  unsigned long long wait_ns = 1000000000ULL;  // bound of every device-side wait (1 s)
+  int skip_first_rung_copy = 0;                // test hook, see fib_attn_plan_set_debug
 };
 
 namespace {
@@ -291,6 +298,12 @@ int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, c
   LayerTable t;
   st = make_table(p, layer, N, p->mode == FIB_MODE_INTERP ? alpha_dev : nullptr, &t);
   if (st != FIB_OK) return st;
+  // bf16 with a window of at most 16 keys: window band on tensor cores (fwd_tc.cu);
+  // otherwise the CUDA-core kernel (fwd.cu), which also serves float32 exactly.
+  if (dtype == FIB_DTYPE_BF16 && tc_supported(t))
+    return cuda_status(launch_fwd_tc(t, B, H, N, q, k, v, o, lse, p->d_lo, p->d_hi, p->d_status,
+                                     p->wait_ns, p->skip_first_rung_copy,
+                                     static_cast<cudaStream_t>(stream)));
   return cuda_status(launch_fwd(t, B, H, N, dtype, q, k, v, o, lse, p->d_lo, p->d_hi,
                                 static_cast<cudaStream_t>(stream)));
 }
@@ -342,6 +355,13 @@ int fib_attn_debug_indices(fib_attn_plan_t p, int layer, int N, int i_begin, int
   if (st != FIB_OK) return st;
   return cuda_status(launch_debug_indices(t, N, i_begin, i_end, out_dev, w_out_dev,
                                           static_cast<cudaStream_t>(stream)));
+}
+
+int fib_attn_plan_set_debug(fib_attn_plan_t p, int skip_first_rung_copy, long long wait_ns) {
+  if (p == nullptr || wait_ns < 1000 || wait_ns > 60LL * 1000000000LL) return FIB_ERR_INVALID_ARG;
+  p->skip_first_rung_copy = skip_first_rung_copy ? 1 : 0;
+  p->wait_ns = static_cast<unsigned long long>(wait_ns);
+  return FIB_OK;
 }
 
 int fib_attn_last_device_status(fib_attn_plan_t p) {

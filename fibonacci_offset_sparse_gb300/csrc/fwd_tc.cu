@@ -1,0 +1,599 @@
+// bf16 forward kernel (sm_103a): window band on tensor cores, rungs on CUDA cores, every
+// K/V row staged into shared memory by the bulk-copy engine.
+//
+// Same operation as fwd.cu ("Depth-Staggered Fibonacci Spacing for Sparse Attention",
+// Methodology > "Attended set", "Scaling", "Implementation"), split by where the work is
+// dense:
+//   * window band: for a warp's 16 consecutive queries every window key lies in the
+//     32-row block [q0-16, q0+16) (W <= 16), so S = Q' K'^T and O = P V run as
+//     mma.sync m16n8k16 (f16 operands, f32 accumulation).  Q' and K' are RoPE-rotated at
+//     their own positions once per staged row; V is staged as f16.
+//   * rungs: a rung is a shifted diagonal (query i reads row i-d); it has no dense block,
+//     so those pairs run on the CUDA cores with packed f32x2 arithmetic, applying RoPE in
+//     relative form: q'_i . k'_{i-d} = sum_m z_m . k_m with z_m the raw query pair rotated
+//     by d theta_m and k_m the raw key pair (rotate-half pairs (m, m+32)).
+//   * data movement: a CTA owns 64 consecutive queries of one (b,h).  The slab a rung needs
+//     is rows [i0-d, i0-d+64) of K and of V: two contiguous 8 KB runs.  One thread issues
+//     cp.async.bulk copies of those runs into a 4-stage shared-memory ring (mbarrier
+//     completion), two rungs ahead of the compute; the raw window rows arrive the same way.
+//     Every mbarrier wait is bounded in time; a wait that gives up records FIB_ERR_TIMEOUT in
+//     the plan's status word, the CTA lets its copies in flight land and exits.
+// Register layout: lane (g = lane/4, t = lane%4) owns query rows g and g+8 of its warp's 16
+// and the dims D_t = [8t, 8t+8) u [32+8t, 32+8t+8) (RoPE partners in the same lane).  The
+// MMA k-order is permuted so that a lane's A/B fragments hold exactly D_t, and V's columns
+// are permuted so that its O accumulator fragment is D_t too: the CUDA-core rung updates
+// and the tensor-core window update share the O registers.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+
+namespace fibattn {
+
+constexpr int kTcWarps = 4;
+constexpr int kTcTile = 16 * kTcWarps;   // queries per CTA
+constexpr int kTcThreads = 32 * kTcWarps;
+constexpr int kWinRows = kTcTile + 16;   // window rows [i0-16, i0+64)
+constexpr int kTcMaxW = 16;
+constexpr int kStages = 4;               // rung slabs resident or in flight
+constexpr int kRungChunk = 2;            // rungs per online-softmax step
+constexpr int kRowBytes = kD * 2;        // one bf16 row
+
+struct TcArgs {
+  LayerTable t;
+  int N;
+  int tiles;
+  int slab_rows;  // 64 (mask) or 72 (interp: 65 rows used)
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  __nv_bfloat16* o;
+  float* lse;
+  const float2* rope_lo;
+  const float2* rope_hi;
+  float qscale;                // log2(e)/sqrt(D)
+  int* status;                 // plan status word (FIB_ERR_TIMEOUT on a wait that gave up)
+  unsigned long long wait_ns;  // bound of every mbarrier wait
+  int skip_first_rung_copy;    // test hook: never arrive on rung 0's stage
+};
+
+// ------------------------------------------------------------------ small PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase of parity `parity` of `bar`, giving up after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 bf2(uint32_t w) { return make_float2(bf_lo(w), bf_hi(w)); }
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* smem_row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(smem_row)));
+}
+
+// e^{i p theta_m} for m = 8t .. 8t+7 at absolute position p.
+__device__ __forceinline__ void abs_factors(const float2* __restrict__ lo_tab,
+                                            const float2* __restrict__ hi_tab, int p, int t,
+                                            float2 (&e)[8]) {
+  const float4* h4 = reinterpret_cast<const float4*>(hi_tab + (p >> 6) * kFreq + 8 * t);
+  const float4* l4 = reinterpret_cast<const float4*>(lo_tab + (p & 63) * kFreq + 8 * t);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float4 a = __ldg(h4 + u), b = __ldg(l4 + u);
+    e[2 * u] = make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
+    e[2 * u + 1] = make_float2(a.z * b.z - a.w * b.w, a.z * b.w + a.w * b.z);
+  }
+}
+
+// Read the 16 dims D_t of a 128-byte bf16 row in shared memory as two 16-byte words;
+// odd rows read their halves in the opposite order, so the 8 lanes of a phase (two rows
+// x four t) hit 8 distinct bank groups.
+__device__ __forceinline__ void lds_row_part(const unsigned char* row, int t, bool odd, uint4& lo,
+                                             uint4& hi) {
+  const uint4* r4 = reinterpret_cast<const uint4*>(row);
+  if (odd) {
+    hi = r4[t + 4];
+    lo = r4[t];
+  } else {
+    lo = r4[t];
+    hi = r4[t + 4];
+  }
+}
+
+// Score partial of one row: sum over the lane's 4 frequency pairs of z1 k1 + z2 k2 with
+// z = q e^{i d theta} (cs = cos, sn = sin of d theta for the lane's frequencies).
+__device__ __forceinline__ float rung_dot(const float2 (&q1)[4], const float2 (&q2)[4],
+                                          const float2 (&cs)[4], const float2 (&sn)[4],
+                                          const uint4& ka, const uint4& kb) {
+  const uint32_t xa[4] = {ka.x, ka.y, ka.z, ka.w}, xb[4] = {kb.x, kb.y, kb.z, kb.w};
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 k1 = bf2(xa[j]), k2 = bf2(xb[j]);
+    const float2 nq2 = make_float2(-q2[j].x, -q2[j].y);
+    const float2 z1 = __ffma2_rn(cs[j], q1[j], __fmul2_rn(sn[j], nq2));
+    const float2 z2 = __ffma2_rn(sn[j], q1[j], __fmul2_rn(cs[j], q2[j]));
+    acc = __ffma2_rn(z1, k1, acc);
+    acc = __ffma2_rn(z2, k2, acc);
+  }
+  return acc.x + acc.y;
+}
+
+__device__ __forceinline__ void load_fac(const float* f, int t, float2 (&cs)[4], float2 (&sn)[4]) {
+  const float4* f4 = reinterpret_cast<const float4*>(f);
+  const float4 ca = f4[2 * t], cb = f4[2 * t + 1], sa = f4[8 + 2 * t], sb = f4[8 + 2 * t + 1];
+  cs[0] = make_float2(ca.x, ca.y);
+  cs[1] = make_float2(ca.z, ca.w);
+  cs[2] = make_float2(cb.x, cb.y);
+  cs[3] = make_float2(cb.z, cb.w);
+  sn[0] = make_float2(sa.x, sa.y);
+  sn[1] = make_float2(sa.z, sa.w);
+  sn[2] = make_float2(sb.x, sb.y);
+  sn[3] = make_float2(sb.z, sb.w);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kTcThreads, 2) fwd_tc_kernel(TcArgs a) {
+  __shared__ KeySmem ks;
+  __shared__ __align__(8) uint64_t bars[kStages + 1];  // rung stages, then the window copy
+  __shared__ volatile int s_err;
+  __shared__ int last_issued[kStages];  // last rung copied into each stage (-1: none)
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int SR = a.slab_rows;
+  const int stage_bytes = 2 * SR * kRowBytes;  // K slab then V slab
+  unsigned char* stages = smem;
+  uint4* Ks = reinterpret_cast<uint4*>(smem + kStages * stage_bytes);  // K' f16, chunk ^ 4(r&1)
+  uint4* Vs = Ks + kWinRows * 8;                                          // V f16 (pi cols), chunk ^ (r&7)
+  float* fac = reinterpret_cast<float*>(Vs + kWinRows * 8);  // per rung: cos[32], sin[32] (x2 interp)
+
+  const int bh = blockIdx.x / a.tiles;
+  const int tile = blockIdx.x - bh * a.tiles;
+  const int i0 = tile * kTcTile;
+  const int N = a.N;
+  const int tid = threadIdx.x;
+  const size_t base = static_cast<size_t>(bh) * N * kD;
+  const __nv_bfloat16* __restrict__ Q = a.q + base;
+  const __nv_bfloat16* __restrict__ K = a.k + base;
+  const __nv_bfloat16* __restrict__ V = a.v + base;
+  const int i_last = min(i0 + kTcTile, N) - 1;  // last real query of the tile
+
+  build_keys(a.t, N, &ks);
+  if (tid == 0) {
+    s_err = 0;
+    for (int s = 0; s < kStages; ++s) last_issued[s] = -1;
+    for (int s = 0; s <= kStages; ++s) mbar_init(&bars[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  const int W = a.t.W;
+  const int nr = ks.nr;
+
+  // slab of rung r: rows [first, first + SR) of K and V, copied where inside [0, N)
+  auto issue_rung = [&](int r) {
+    const int s = r % kStages;
+    if (r == 0 && a.skip_first_rung_copy) return;  // test hook: the stage never completes
+    last_issued[s] = r;
+    const int lo = ks.lo[W + r];
+    const int first = i0 - lo - (MODE == 1 ? 1 : 0);
+    const int r0 = max(first, 0);
+    const int r1 = i_last - lo + 1;  // rows read by the tile's real queries end here
+    const uint32_t bytes = r1 > r0 ? static_cast<uint32_t>(r1 - r0) * kRowBytes : 0u;
+    mbar_arrive_tx(&bars[s], 2 * bytes);
+    if (bytes) {
+      unsigned char* dst = stages + s * stage_bytes + (r0 - first) * kRowBytes;
+      bulk_g2s(dst, K + static_cast<size_t>(r0) * kD, bytes, &bars[s]);
+      bulk_g2s(dst + SR * kRowBytes, V + static_cast<size_t>(r0) * kD, bytes, &bars[s]);
+    }
+  };
+
+  // ---- copies: raw window rows into the areas of stages 2 and 3, rungs 0 and 1
+  if (tid == 0) {
+    const int w0 = max(i0 - 16, 0), w1 = i_last + 1;
+    const uint32_t bytes = static_cast<uint32_t>(w1 - w0) * kRowBytes;
+    mbar_arrive_tx(&bars[kStages], 2 * bytes);
+    bulk_g2s(stages + 2 * stage_bytes + (w0 - (i0 - 16)) * kRowBytes, K + static_cast<size_t>(w0) * kD,
+             bytes, &bars[kStages]);
+    bulk_g2s(stages + 3 * stage_bytes + (w0 - (i0 - 16)) * kRowBytes, V + static_cast<size_t>(w0) * kD,
+             bytes, &bars[kStages]);
+    for (int r = 0; r < min(nr, 2); ++r) issue_rung(r);
+  }
+
+  // ---- rung relative factors: cos / sin of lo*theta (and (lo+1)*theta for interp)
+  for (int idx = tid; idx < nr * kFreq; idx += kTcThreads) {
+    const int r = idx / kFreq, m = idx % kFreq;
+    const int lo = ks.lo[W + r];
+    const float2 e = rope_factor(a.rope_lo, a.rope_hi, lo, m);
+    fac[r * 64 + m] = e.x;
+    fac[r * 64 + 32 + m] = e.y;
+    if (MODE == 1) {
+      const float2 e1 = rope_factor(a.rope_lo, a.rope_hi, lo + 1, m);
+      fac[(kMaxR + r) * 64 + m] = e1.x;
+      fac[(kMaxR + r) * 64 + 32 + m] = e1.y;
+    }
+  }
+
+  // ---- per-lane query state
+  const int warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int q0 = i0 + 16 * warp;
+  int irow[2];
+  float2 q1[2][4], q2[2][4];  // raw q * qscale: (dims 8t+2j, 8t+2j+1) and their partners
+  uint32_t qa[2][2][4];       // A fragments: [row h][dim half][k-step]
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = q0 + g + 8 * h;
+    irow[h] = i;
+    const int ic = i < N ? i : N - 1;
+    float x[16];
+    load_part(Q + static_cast<size_t>(ic) * kD, t, x);
+#pragma unroll
+    for (int u = 0; u < 16; ++u) x[u] *= a.qscale;
+    float2 e[8];
+    abs_factors(a.rope_lo, a.rope_hi, ic, t, e);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      q1[h][j] = make_float2(x[2 * j], x[2 * j + 1]);
+      q2[h][j] = make_float2(x[8 + 2 * j], x[8 + 2 * j + 1]);
+    }
+    float y[16];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      y[u] = x[u] * e[u].x - x[8 + u] * e[u].y;
+      y[8 + u] = x[u] * e[u].y + x[8 + u] * e[u].x;
+    }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      qa[h][0][s] = pack_h2(y[2 * s], y[2 * s + 1]);
+      qa[h][1][s] = pack_h2(y[8 + 2 * s], y[8 + 2 * s + 1]);
+    }
+  }
+
+  // ---- window rows: raw bf16 (stages 2/3 areas) -> K' f16 rotated, V f16 permuted
+  if (!mbar_wait(&bars[kStages], 0, a.wait_ns)) s_err = 1;  // (every thread waits here)
+  {
+    const unsigned char* kraw = stages + 2 * stage_bytes;
+    const unsigned char* vraw = stages + 3 * stage_bytes;
+    for (int task = tid; task < kWinRows * 4; task += kTcThreads) {
+      const int row = task >> 2, c = task & 3;
+      const int p = i0 - 16 + row;
+      uint4 lo4 = make_uint4(0, 0, 0, 0), hi4 = make_uint4(0, 0, 0, 0);
+      if (p >= 0 && p < N && !s_err) {
+        const uint4* r4 = reinterpret_cast<const uint4*>(kraw + row * kRowBytes);
+        const uint4 wa = r4[c], wb = r4[c + 4];
+        const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w}, xb[4] = {wb.x, wb.y, wb.z, wb.w};
+        float2 e[8];
+        abs_factors(a.rope_lo, a.rope_hi, p, c, e);
+        uint32_t ya[4], yb[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 k1 = bf2(xa[j]), k2 = bf2(xb[j]);
+          const float2 e0 = e[2 * j], e1 = e[2 * j + 1];
+          ya[j] = pack_h2(k1.x * e0.x - k2.x * e0.y, k1.y * e1.x - k2.y * e1.y);
+          yb[j] = pack_h2(k1.x * e0.y + k2.x * e0.x, k1.y * e1.y + k2.y * e1.x);
+        }
+        lo4 = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+        hi4 = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+      }
+      const int sw = (row & 1) * 4;
+      Ks[row * 8 + (c ^ sw)] = lo4;
+      Ks[row * 8 + ((c + 4) ^ sw)] = hi4;
+    }
+    // V: dim 32h + 8t + u  ->  column 8 (4h + u/2) + 2t + (u%2)
+    for (int task = tid; task < kWinRows * 8; task += kTcThreads) {
+      const int row = task >> 3, c8 = task & 7;
+      const int p = i0 - 16 + row;
+      const int hh = c8 >> 2, tt = c8 & 3;
+      uint32_t w[4] = {0, 0, 0, 0};
+      if (p >= 0 && p < N && !s_err) {
+        const uint4 raw = reinterpret_cast<const uint4*>(vraw + row * kRowBytes)[c8];
+        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = pack_h2(bf_lo(rw[j]), bf_hi(rw[j]));
+      }
+      uint32_t* vrow = reinterpret_cast<uint32_t*>(Vs + row * 8);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) vrow[((4 * hh + j) ^ (row & 7)) * 4 + tt] = w[j];
+    }
+  }
+  __syncthreads();  // Ks, Vs, fac ready; stages 2 and 3 free
+  if (tid == 0 && !s_err)
+    for (int r = 2; r < min(nr, 4); ++r) issue_rung(r);
+
+  // ---- window: S = Q' K'^T over keys [q0-16, q0+16)
+  float S[4][4];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) S[nt][u] = 0.f;
+    const int row = 16 * warp + 8 * nt + g;
+    const int sw = (row & 1) * 4;
+    const uint4 klo = Ks[row * 8 + (t ^ sw)];
+    const uint4 khi = Ks[row * 8 + ((t + 4) ^ sw)];
+    const uint32_t kl[4] = {klo.x, klo.y, klo.z, klo.w};
+    const uint32_t kh[4] = {khi.x, khi.y, khi.z, khi.w};
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      mma16816(S[nt], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
+  }
+  // mask: query row rr = g + 8h, key column c = 8nt + 2t + e  ->  distance rr + 16 - c
+  float m[2], lw[2], lr[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int c = 8 * nt + 2 * t + e;
+        const int dist = g + 8 * h + 16 - c;
+        const bool ok = dist >= 0 && dist < W && q0 - 16 + c >= 0;
+        float& s = S[nt][2 * h + e];
+        s = ok ? s : -INFINITY;
+        mx = fmaxf(mx, s);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    m[h] = mx;  // finite: distance 0 (the query itself) is always in the block
+    float sum = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float& s = S[nt][2 * h + e];
+        s = exp2f(s - mx);
+        sum += s;
+      }
+    lw[h] = sum;  // lane-partial window sum
+    lr[h] = 0.f;  // rung sum (the same in the 4 lanes of a quad)
+  }
+  // ---- window: O = P V
+  float2 O[8][2];  // [n-tile nd][row h] = dims (2nd, 2nd+1) of D_t
+#pragma unroll
+  for (int nd = 0; nd < 8; ++nd) O[nd][0] = O[nd][1] = make_float2(0.f, 0.f);
+  {
+    const int mi = lane >> 3, rl = lane & 7;
+#pragma unroll
+    for (int s2 = 0; s2 < 2; ++s2) {
+      const uint32_t pa0 = pack_h2(S[2 * s2][0], S[2 * s2][1]);
+      const uint32_t pa1 = pack_h2(S[2 * s2][2], S[2 * s2][3]);
+      const uint32_t pa2 = pack_h2(S[2 * s2 + 1][0], S[2 * s2 + 1][1]);
+      const uint32_t pa3 = pack_h2(S[2 * s2 + 1][2], S[2 * s2 + 1][3]);
+      const int vrow = 16 * warp + 16 * s2 + (mi & 1) * 8 + rl;
+#pragma unroll
+      for (int nd = 0; nd < 8; nd += 2) {
+        const int ch = (nd + (mi >> 1)) ^ (vrow & 7);
+        uint32_t b[4];
+        ldsm_x4_trans(b, Vs + vrow * 8 + ch);
+        float c0[4] = {O[nd][0].x, O[nd][0].y, O[nd][1].x, O[nd][1].y};
+        float c1[4] = {O[nd + 1][0].x, O[nd + 1][0].y, O[nd + 1][1].x, O[nd + 1][1].y};
+        mma16816(c0, pa0, pa1, pa2, pa3, b[0], b[1]);
+        mma16816(c1, pa0, pa1, pa2, pa3, b[2], b[3]);
+        O[nd][0] = make_float2(c0[0], c0[1]);
+        O[nd][1] = make_float2(c0[2], c0[3]);
+        O[nd + 1][0] = make_float2(c1[0], c1[1]);
+        O[nd + 1][1] = make_float2(c1[2], c1[3]);
+      }
+    }
+  }
+
+  // ---- rungs: chunks of kRungChunk, online softmax, slabs from the stage ring
+  int ic[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) ic[h] = irow[h] < N ? irow[h] : N - 1;
+  for (int r0 = 0; r0 < nr; r0 += kRungChunk) {
+    float sc[2][kRungChunk];
+#pragma unroll
+    for (int cc = 0; cc < kRungChunk; ++cc) {
+      const int r = r0 + cc;
+      const bool in = r < nr;
+      const int c = W + r;
+      const int s = r % kStages;
+      if (in && !s_err && !mbar_wait(&bars[s], (r / kStages) & 1, a.wait_ns)) s_err = 1;
+      const bool live = in && !s_err;
+      const int lo = in ? ks.lo[c] : 0;
+      const int need = in ? ks.need[c] : 0x7fffffff;
+      const float w = (MODE == 1 && in) ? ks.w[c] : 0.f;
+      const int first = i0 - lo - (MODE == 1 ? 1 : 0);
+      const unsigned char* kst = stages + s * stage_bytes;
+      float2 cs[4], sn[4];
+      if (live) load_fac(fac + r * 64, t, cs, sn);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const bool ok = live && ic[h] >= need;
+        float part = 0.f;
+        if (ok) {
+          const int row = ic[h] - lo - first;
+          uint4 ka, kb;
+          lds_row_part(kst + row * kRowBytes, t, row & 1, ka, kb);
+          part = rung_dot(q1[h], q2[h], cs, sn, ka, kb);
+          if (MODE == 1 && w > 0.f) {
+            float2 c2[4], s2[4];
+            load_fac(fac + (kMaxR + r) * 64, t, c2, s2);
+            lds_row_part(kst + (row - 1) * kRowBytes, t, (row - 1) & 1, ka, kb);
+            part = (1.f - w) * part + w * rung_dot(q1[h], q2[h], c2, s2, ka, kb);
+          }
+        }
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        sc[h][cc] = ok ? part : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float mc = m[h];
+#pragma unroll
+      for (int cc = 0; cc < kRungChunk; ++cc) mc = fmaxf(mc, sc[h][cc]);
+      const float corr = exp2f(m[h] - mc);
+      m[h] = mc;
+      lw[h] *= corr;
+      lr[h] *= corr;
+      const float2 corr2 = make_float2(corr, corr);
+#pragma unroll
+      for (int nd = 0; nd < 8; ++nd) O[nd][h] = __fmul2_rn(O[nd][h], corr2);
+#pragma unroll
+      for (int cc = 0; cc < kRungChunk; ++cc) {
+        const float p = exp2f(sc[h][cc] - mc);
+        lr[h] += p;
+        if (p > 0.f) {
+          const int r = r0 + cc;
+          const int c = W + r;
+          const int lo = ks.lo[c];
+          const float w = MODE == 1 ? ks.w[c] : 0.f;
+          const int first = i0 - lo - (MODE == 1 ? 1 : 0);
+          const int row = ic[h] - lo - first;
+          const unsigned char* vst = stages + (r % kStages) * stage_bytes + SR * kRowBytes;
+          uint4 va, vb;
+          lds_row_part(vst + row * kRowBytes, t, row & 1, va, vb);
+          const uint32_t xa[4] = {va.x, va.y, va.z, va.w}, xb[4] = {vb.x, vb.y, vb.z, vb.w};
+          const float p0 = p * (1.f - w);
+          const float2 pp = make_float2(p0, p0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            O[j][h] = __ffma2_rn(pp, bf2(xa[j]), O[j][h]);
+            O[4 + j][h] = __ffma2_rn(pp, bf2(xb[j]), O[4 + j][h]);
+          }
+          if (MODE == 1 && w > 0.f) {
+            lds_row_part(vst + (row - 1) * kRowBytes, t, (row - 1) & 1, va, vb);
+            const uint32_t ya[4] = {va.x, va.y, va.z, va.w}, yb[4] = {vb.x, vb.y, vb.z, vb.w};
+            const float2 pw = make_float2(p * w, p * w);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              O[j][h] = __ffma2_rn(pw, bf2(ya[j]), O[j][h]);
+              O[4 + j][h] = __ffma2_rn(pw, bf2(yb[j]), O[4 + j][h]);
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();  // every warp is done with these stages
+    if (tid == 0 && !s_err)
+      for (int r = r0 + kStages; r < min(nr, r0 + kStages + kRungChunk); ++r) issue_rung(r);
+  }
+
+  // ---- epilogue
+  if (s_err) {
+    if (tid == 0) {
+      atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
+      // only the last copy issued into a stage can still be in flight; a phase that has
+      // completed already satisfies its parity wait at once (each wait is bounded)
+      mbar_wait(&bars[kStages], 0, a.wait_ns);
+      for (int s = 0; s < kStages; ++s)
+        if (last_issued[s] >= 0) mbar_wait(&bars[s], (last_issued[s] / kStages) & 1, a.wait_ns);
+    }
+    return;
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float l = lw[h];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    l += lr[h];
+    const int i = irow[h];
+    if (i < N) {
+      const float inv = 1.f / l;
+      float ov[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        ov[2 * j] = O[j][h].x * inv;
+        ov[2 * j + 1] = O[j][h].y * inv;
+        ov[8 + 2 * j] = O[4 + j][h].x * inv;
+        ov[8 + 2 * j + 1] = O[4 + j][h].y * inv;
+      }
+      store_part(a.o + base + static_cast<size_t>(i) * kD, t, ov);
+      if (t == 0 && a.lse != nullptr) a.lse[static_cast<size_t>(bh) * N + i] = (m[h] + log2f(l)) * kLn2;
+    }
+  }
+}
+
+bool tc_supported(const LayerTable& t) { return t.W <= kTcMaxW; }
+
+static size_t tc_smem_bytes(int mode, int slab_rows) {
+  return static_cast<size_t>(kStages) * 2 * slab_rows * kRowBytes + 2 * kWinRows * 8 * sizeof(uint4) +
+         static_cast<size_t>(mode == 1 ? 2 : 1) * kMaxR * 64 * sizeof(float);
+}
+
+cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k,
+                          const void* v, void* o, float* lse, const float2* lo_tab,
+                          const float2* hi_tab, int* status, unsigned long long wait_ns,
+                          int skip_first_rung_copy, cudaStream_t stream) {
+  TcArgs a;
+  a.t = t;
+  a.N = N;
+  a.tiles = (N + kTcTile - 1) / kTcTile;
+  a.slab_rows = t.mode == 1 ? 72 : 64;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.rope_lo = lo_tab;
+  a.rope_hi = hi_tab;
+  a.qscale = kLog2e / 8.0f;
+  a.status = status;
+  a.wait_ns = wait_ns;
+  a.skip_first_rung_copy = skip_first_rung_copy;
+  const long long blocks = static_cast<long long>(a.tiles) * B * H;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const size_t smem = tc_smem_bytes(t.mode, a.slab_rows);
+  cudaError_t e;
+  if (t.mode == 0) {
+    e = cudaFuncSetAttribute(fwd_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    fwd_tc_kernel<0><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a);
+  } else {
+    e = cudaFuncSetAttribute(fwd_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    fwd_tc_kernel<1><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fibattn

@@ -27,7 +27,7 @@ EXPORTS = [
     "fib_attn_error_string", "fib_attn_base", "fib_attn_schedule", "fib_attn_mask_distances",
     "fib_attn_interp_rungs", "fib_attn_plan_create", "fib_attn_plan_destroy",
     "fib_attn_plan_distances", "fib_attn_fwd", "fib_attn_bwd_workspace_size", "fib_attn_bwd",
-    "fib_attn_debug_indices", "fib_attn_last_device_status",
+    "fib_attn_debug_indices", "fib_attn_last_device_status", "fib_attn_plan_set_debug",
 ]
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -53,6 +53,7 @@ _SIGS = {
                           _vp, _vp, ctypes.c_size_t, _vp]),
     "fib_attn_debug_indices": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "fib_attn_last_device_status": (_i, [_vp]),
+    "fib_attn_plan_set_debug": (_i, [_vp, _i, ctypes.c_longlong]),
 }
 
 _lib = None
@@ -243,6 +244,11 @@ def fib_attn_debug_indices(plan: Plan, layer: int, N: int, i_begin: int, i_end: 
     _check("fib_attn_debug_indices", lib().fib_attn_debug_indices(
         plan.handle, layer, N, i_begin, i_end, _ptr(out), _ptr(w), _ptr(alpha_dev), _stream(stream)))
     return out, w
+
+
+def fib_attn_plan_set_debug(plan: Plan, skip_first_rung_copy: bool, wait_ns: int):
+    _check("fib_attn_plan_set_debug", lib().fib_attn_plan_set_debug(
+        plan.handle, 1 if skip_first_rung_copy else 0, int(wait_ns)))
 
 
 def fib_attn_last_device_status(plan: Plan) -> int:

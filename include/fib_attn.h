@@ -158,6 +158,15 @@ int fib_attn_debug_indices(fib_attn_plan_t p, int layer, int N, int i_begin, int
                            int32_t* out_dev, float* w_out_dev, const float* alpha_dev,
                            void* stream);
 
+/* Wait bound and fault-injection hook of the plan's kernels.  Kernels that stage rows with
+ * the bulk-copy engine wait on mbarriers; every such wait gives up after wait_ns
+ * nanoseconds (default 1e9; accepted range [1e3, 6e10]), records FIB_ERR_TIMEOUT in the
+ * status word, lets the copies already in flight land and returns without writing output.
+ * skip_first_rung_copy != 0 makes the bf16 forward never complete its first rung stage, so
+ * that a test can drive that timeout path without any device fault.  Host-only; takes
+ * effect on the next launch.  FIB_ERR_INVALID_ARG on a null plan or wait_ns out of range.   */
+int fib_attn_plan_set_debug(fib_attn_plan_t p, int skip_first_rung_copy, long long wait_ns);
+
 /* Synchronises the plan's device, then returns and clears the device status word:
  * FIB_OK, FIB_ERR_TIMEOUT (a bounded wait gave up) or FIB_ERR_DEVICE_ASSERT.          */
 int fib_attn_last_device_status(fib_attn_plan_t p);

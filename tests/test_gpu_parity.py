@@ -5,10 +5,15 @@ Tolerances:
   * O: max-abs <= 1e-5 for float32 inputs; <= 1e-2 for bf16 inputs (float32 accumulation)
     against the oracle run on the same bf16-rounded values, plus the bf16 output's own
     rounding (at most half an ulp, bounded by 2^-8 |O|);
-  * LSE (float32 output): 1e-5 (float32 inputs), 1e-3 (bf16 inputs);
+  * LSE (float32 output): 1e-5 (float32 inputs); 5e-3 for bf16 inputs: the tensor-core
+    window rounds the RoPE-rotated Q' and K' to f16 (11-bit significand), so a 64-term
+    score carries up to ~1e-3 of rounding error, which LSE inherits (the O bound above
+    is the binding one);
   * dQ, dK, dV, dalpha: relative L2 <= 2e-2.
 """
+import json
 import math
+import os
 
 import numpy as np
 import pytest
@@ -50,9 +55,21 @@ def _plan(kind, alphas, W, N_max, mode):
     return fa.fib_attn_plan_create(bk, alphas, W, N_max, m, custom_base=custom)
 
 
+_LOG = os.environ.get("FIB_PARITY_LOG")
+
+
+def _record(kind, what, value):
+    if _LOG:
+        with open(_LOG, "a") as f:
+            f.write(json.dumps({"check": kind, "case": what, "value": float(value)}) + "\n")
+
+
 def _check_o(o_gpu, O_ref, dtype, what=""):
     og = o_gpu.detach().double().cpu().numpy()
     err = np.abs(og - O_ref)
+    _record("o_maxabs_" + dtype, what, err.max())
+    if dtype != "f32":
+        _record("o_excess_over_rounding_" + dtype, what, (err - np.abs(O_ref) * 2.0 ** -8).max())
     if dtype == "f32":
         assert err.max() <= F32_ATOL, f"{what} max-abs {err.max():.3e}"
     else:
@@ -63,8 +80,9 @@ def _check_o(o_gpu, O_ref, dtype, what=""):
 
 def _check_lse(lse_gpu, lse_ref, dtype, what=""):
     lg = lse_gpu.detach().double().cpu().numpy()
-    tol = 1e-5 if dtype == "f32" else 1e-3
+    tol = 1e-5 if dtype == "f32" else 5e-3
     err = np.abs(lg - lse_ref).max()
+    _record("lse_maxabs_" + dtype, what, err)
     assert err <= tol, f"{what} lse max-abs {err:.3e}"
 
 
@@ -139,8 +157,10 @@ def test_c3_learned_fwd_bwd_bf16():
         rq, rk, rv, ra = oracle.attend_bwd(qf, kf, vf, gf, a, oracle.fibonacci_base(), W, "interp")
         for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
             e = _rel_l2(g.double().cpu().numpy(), r)
+            _record("bwd_rel_l2_" + name, f"c3 layer {layer}", e)
             assert e <= REL_L2, f"layer {layer} {name} rel-L2 {e:.3e}"
         e = abs(float(da.item()) - ra) / max(abs(ra), 1e-30)
+        _record("bwd_rel_dalpha", f"c3 layer {layer}", e)
         assert e <= REL_L2, f"layer {layer} dalpha {da.item()} vs {ra} rel {e:.3e}"
     plan.close()
 
@@ -279,4 +299,55 @@ def test_device_error_paths():
     assert lib.fib_attn_bwd(*bad, ws_need, s) == fa.FIB_ERR_INVALID_ARG        # misaligned ws
     assert lib.fib_attn_bwd(*args, ws_need, s) == fa.FIB_OK
     assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    plan.close()
+
+
+# ------------------------------------------------------------------ edge cases, bf16
+@pytest.mark.parametrize("mode", ["mask", "interp"])
+@pytest.mark.parametrize("N,W,alpha,kind", [
+    (1, 12, 1.0, "fib"),            # a single query
+    (15, 12, 1.3, "fib"),           # less than one warp tile
+    (65, 16, 0.5, "fib"),           # widest window on tensor cores; ragged tail of 1
+    (77, 17, 0.9, "fib"),           # W = 17: CUDA-core kernel
+    (200, 1, 1.5, "fib"),           # window of one
+    (333, 8, 1.2345, "pow2"),
+    (150, 4, 1.0, (37,)),
+    (1000, 12, 1.4999, "fib"),      # rungs reaching across several 64-query tiles
+])
+def test_edge_cases_bf16(mode, N, W, alpha, kind):
+    B, H = 2, 3
+    plan = _plan(kind, [alpha], W, N, mode)
+    q, k, v = inputs.qkv(B, H, N, 64, 300 + N, W, "bf16")
+    o, lse = fa.fib_attn_fwd(plan, 0, q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    O_ref, lse_ref = oracle.attend(inputs.as_f64(q), inputs.as_f64(k), inputs.as_f64(v), alpha,
+                                   _base_fn(kind)(N), W, mode)
+    _check_o(o, O_ref, "bf16", f"edge N={N} W={W} {mode}")
+    _check_lse(lse, lse_ref, "bf16")
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    plan.close()
+
+
+# ------------------------------------------------------------------ bounded waits
+def test_starved_stage_times_out_and_context_survives():
+    """The hook leaves the first rung stage of every CTA without its copy; each CTA's wait
+    gives up after 2 ms, records FIB_ERR_TIMEOUT and exits.  The same context then runs a
+    normal forward that matches the oracle."""
+    B, H, N, W, alpha = 1, 2, 256, 12, 1.0
+    plan = _plan("fib", [alpha], W, N, "mask")
+    q, k, v = inputs.qkv(B, H, N, 64, 500, 0, "bf16")
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    fa.fib_attn_plan_set_debug(plan, True, 2_000_000)
+    fa.fib_attn_fwd(plan, 0, qc, kc, vc)
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_ERR_TIMEOUT
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK  # reading clears it
+    fa.fib_attn_plan_set_debug(plan, False, 1_000_000_000)
+    o, lse = fa.fib_attn_fwd(plan, 0, qc, kc, vc)
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    O_ref, lse_ref = oracle.attend(inputs.as_f64(q), inputs.as_f64(k), inputs.as_f64(v), alpha,
+                                   oracle.fibonacci_base(), W, "mask")
+    _check_o(o, O_ref, "bf16", "after timeout")
+    with pytest.raises(fa.FibAttnError):
+        fa.fib_attn_plan_set_debug(plan, False, 10)
     plan.close()
