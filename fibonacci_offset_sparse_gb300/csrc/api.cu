@@ -31,6 +31,8 @@ cudaError_t launch_bwd(const LayerTable& t, int B, int H, int N, int dtype, cons
                        const void* k, const void* v, const void* o, const float* lse,
                        const void* dO, void* dq, void* dk, void* dv, float* dalpha, void* ws,
                        const float2* lo_tab, const float2* hi_tab, cudaStream_t stream);
+cudaError_t noalloc_scratch(void** out);
+size_t noalloc_scratch_bytes();
 }  // namespace fibattn
 
 using namespace fibattn;
@@ -339,6 +341,40 @@ int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, c
   if (st != FIB_OK) return st;
   return cuda_status(launch_bwd(t, B, H, N, dtype, q, k, v, o, lse, dO, dq, dk, dv, dalpha,
                                 workspace, p->d_lo, p->d_hi, static_cast<cudaStream_t>(stream)));
+}
+
+// Backward for callers that cannot allocate device memory: the same checks and kernels as
+// fib_attn_bwd, but the scratch is the library's fixed device array (bwd.cu), so the caller
+// passes no workspace and nothing is allocated here.
+int fib_attn_bwd_noalloc(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
+                         const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                         float* dalpha, const float* alpha_dev, void* stream) {
+  int st = check_shape(p, layer, B, H, N, dtype);
+  if (st != FIB_OK) return st;
+  if (check_tensor(q) || check_tensor(k) || check_tensor(v) || check_tensor(o) ||
+      check_tensor(dO) || check_tensor(dq) || check_tensor(dk) || check_tensor(dv))
+    return FIB_ERR_INVALID_ARG;
+  if (lse == nullptr || !aligned(lse, 4) || dalpha == nullptr || !aligned(dalpha, 4)) return FIB_ERR_INVALID_ARG;
+  if (alpha_dev != nullptr && !aligned(alpha_dev, 4)) return FIB_ERR_INVALID_ARG;
+  const void* ins[] = {q, k, v, o, dO};
+  const void* outs[] = {dq, dk, dv};
+  for (const void* a : outs)
+    for (const void* b : ins)
+      if (a == b) return FIB_ERR_INVALID_ARG;
+  if (dq == dk || dq == dv || dk == dv) return FIB_ERR_INVALID_ARG;
+  // the whole scratch of this call must fit the fixed array
+  if (bwd_workspace_bytes(B, H, N) > noalloc_scratch_bytes()) return FIB_ERR_INVALID_ARG;
+  st = check_device(p);
+  if (st != FIB_OK) return st;
+  LayerTable t;
+  st = make_table(p, layer, N, p->mode == FIB_MODE_INTERP ? alpha_dev : nullptr, &t);
+  if (st != FIB_OK) return st;
+  void* scratch = nullptr;
+  const cudaError_t e = noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_bwd(t, B, H, N, dtype, q, k, v, o, lse, dO, dq, dk, dv, dalpha,
+                                scratch, p->d_lo, p->d_hi, static_cast<cudaStream_t>(stream)));
 }
 
 int fib_attn_debug_indices(fib_attn_plan_t p, int layer, int N, int i_begin, int i_end,

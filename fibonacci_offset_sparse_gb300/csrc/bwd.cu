@@ -14,6 +14,8 @@
 //   dalpha = fixed-order sum of the CTA partials          (dalpha_reduce_kernel)
 // Both main kernels recompute scores from raw Q/K with the relative RoPE factors
 // (see fwd.cu), so no attention matrix is stored.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace fibattn {
@@ -317,5 +319,47 @@ cudaError_t launch_bwd(const LayerTable& t, int B, int H, int N, int dtype, cons
   dalpha_reduce_kernel<<<1, 256, 0, stream>>>(a.partials, static_cast<int>(blocks), dalpha, t.mode);
   return cudaGetLastError();
 }
+
+// ---------------------------------------------------------------------------------------
+// Backward without any allocation: the scratch lives in a fixed, file-scope device array.
+//
+// Some callers must not allocate device memory on the call path: a plugin inside a host
+// framework that owns the whole device heap, or a real-time loop with a no-allocation
+// rule.  They cannot hand fib_attn_bwd a workspace of their own, so fib_attn_bwd_noalloc
+// uses the array below instead.  The array is kNoAllocScratchBytes (8 MiB) on every device
+// that loads the library, held until the process exits.  Every call shares it and it keeps
+// the last call's contents; nothing in it needs to start at zero (Delta and the dalpha
+// partials are fully written before they are read).  Two calls whose kernels overlap on the
+// GPU (different streams without ordering) race on the array.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kNoAllocMaxDevices] = {};
+}  // namespace
+
+// Device address of the scratch array on the current device.  In host code the array's
+// name is only a host-side stand-in, never a device address, so the first call on a device
+// looks the address up with cudaGetSymbolAddress (with that device current) and caches it;
+// later calls on that device reuse the cached pointer.
+cudaError_t noalloc_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_bwd_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 
 }  // namespace fibattn

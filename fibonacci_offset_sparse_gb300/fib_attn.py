@@ -28,6 +28,7 @@ EXPORTS = [
     "fib_attn_interp_rungs", "fib_attn_plan_create", "fib_attn_plan_destroy",
     "fib_attn_plan_distances", "fib_attn_fwd", "fib_attn_bwd_workspace_size", "fib_attn_bwd",
     "fib_attn_debug_indices", "fib_attn_last_device_status", "fib_attn_plan_set_debug",
+    "fib_attn_bwd_noalloc",
 ]
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -54,6 +55,8 @@ _SIGS = {
     "fib_attn_debug_indices": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "fib_attn_last_device_status": (_i, [_vp]),
     "fib_attn_plan_set_debug": (_i, [_vp, _i, ctypes.c_longlong]),
+    "fib_attn_bwd_noalloc": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                  _vp, _vp, _vp, _vp]),
 }
 
 _lib = None
@@ -233,6 +236,18 @@ def fib_attn_bwd(plan: Plan, layer: int, q, k, v, o, lse, dO, dq=None, dk=None, 
         plan.handle, layer, B, H, N, _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
         _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _ptr(alpha_dev), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dq, dk, dv, dalpha
+
+
+def fib_attn_bwd_noalloc(plan: Plan, layer: int, q, k, v, o, lse, dO, dq, dk, dv, dalpha,
+                         alpha_dev=None, stream=None):
+    """Backward into caller-provided dq, dk, dv, dalpha[1] with the library's fixed scratch
+    array: no workspace argument and nothing allocated (for callers that may not allocate)."""
+    B, H, N = _shape(q)
+    _same(q, k, v, o, dO, dq, dk, dv)
+    _check("fib_attn_bwd_noalloc", lib().fib_attn_bwd_noalloc(
+        plan.handle, layer, B, H, N, _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+        _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _ptr(alpha_dev), _stream(stream)))
     return dq, dk, dv, dalpha
 
 

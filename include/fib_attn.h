@@ -148,6 +148,23 @@ int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
                  float* dalpha, const float* alpha_dev, void* workspace, size_t ws_bytes,
                  void* stream);
 
+/* Backward without allocation.  The paper has no counterpart: this is an interface for
+ * callers that cannot allocate device memory on the call path -- for example a plugin inside
+ * a framework that owns the device heap, or a real-time loop that forbids allocation -- and
+ * so cannot hand fib_attn_bwd a workspace.  Same arguments, results and errors as
+ * fib_attn_bwd without workspace/ws_bytes: the scratch is a fixed 8 MiB device array inside
+ * the library, held on every device that loads it until the process exits.  A call needing
+ * more (fib_attn_bwd_workspace_size(p, B, H, N) > 8 MiB, i.e. B*H*N above about two
+ * million) returns FIB_ERR_INVALID_ARG before any launch.  The first call on a device looks
+ * up the array's device address and caches it (host-side work; make that first call before
+ * any stream capture).  Every call shares the array and it keeps the last call's contents
+ * (nothing in it needs zeroing); calls whose kernels overlap on the GPU race on it.  Nothing
+ * is allocated, by the library or through CUDA.                                           */
+int fib_attn_bwd_noalloc(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
+                         const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                         float* dalpha, const float* alpha_dev, void* stream);
+
 /* ---------------------------------------------------------------- debug / status ----
  * The attended index sets of queries [i_begin, i_end), produced by the same device
  * index code as the forward kernel.  out_dev: int32 [(i_end-i_begin), W + FIB_MAX_RUNGS]
