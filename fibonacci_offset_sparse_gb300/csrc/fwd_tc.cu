@@ -12,12 +12,16 @@
 //     so those pairs run on the CUDA cores with packed f32x2 arithmetic, applying RoPE in
 //     relative form: q'_i . k'_{i-d} = sum_m z_m . k_m with z_m the raw query pair rotated
 //     by d theta_m and k_m the raw key pair (rotate-half pairs (m, m+32)).
-//   * data movement: a CTA owns 64 consecutive queries of one (b,h).  The slab a rung needs
-//     is rows [i0-d, i0-d+64) of K and of V: two contiguous 8 KB runs.  One thread issues
-//     cp.async.bulk copies of those runs into a 4-stage shared-memory ring (mbarrier
-//     completion), two rungs ahead of the compute; the raw window rows arrive the same way.
-//     Every mbarrier wait is bounded in time; a wait that gives up records FIB_ERR_TIMEOUT in
-//     the plan's status word, the CTA lets its copies in flight land and exits.
+//   * data movement: a CTA owns 64 consecutive queries of one (b,h) and is warp-specialised:
+//     4 consumer warps compute, 1 producer thread streams every row they read through a
+//     4-slot shared-memory ring with cp.async.bulk (mbarrier completion): the Q rows, the
+//     raw window K and V rows [i0-16, i0+64), then per rung the slab rows [i0-d, i0-d+64)
+//     of K and V (two contiguous runs).  The producer runs up to 4 slots ahead and refills a
+//     slot as soon as the 4 consumer warps release it; the window rows are converted in
+//     place inside their slots, so the ring is nearly all of the CTA's shared memory and 3
+//     CTAs fit on an SM.  Every mbarrier wait is bounded in time; a wait that gives up
+//     records FIB_ERR_TIMEOUT in the plan's status word, the consumers stop, and the producer
+//     lets its copies in flight land before the CTA exits.
 // Register layout: lane (g = lane/4, t = lane%4) owns query rows g and g+8 of its warp's 16
 // and the dims D_t = [8t, 8t+8) u [32+8t, 32+8t+8) (RoPE partners in the same lane).  The
 // MMA k-order is permuted so that a lane's A/B fragments hold exactly D_t, and V's columns
@@ -29,20 +33,23 @@
 
 namespace fibattn {
 
-constexpr int kTcWarps = 4;
-constexpr int kTcTile = 16 * kTcWarps;   // queries per CTA
-constexpr int kTcThreads = 32 * kTcWarps;
-constexpr int kWinRows = kTcTile + 16;   // window rows [i0-16, i0+64)
+constexpr int kTcWarps = 4;                    // consumer warps
+constexpr int kTcTile = 16 * kTcWarps;         // queries per CTA
+constexpr int kConsumers = 32 * kTcWarps;
+constexpr int kTcThreads = kConsumers + 32;    // + one producer warp
+constexpr int kWinRows = kTcTile + 16;         // window rows [i0-16, i0+64)
 constexpr int kTcMaxW = 16;
-constexpr int kStages = 4;               // rung slabs resident or in flight
-constexpr int kRungChunk = 2;            // rungs per online-softmax step
-constexpr int kRowBytes = kD * 2;        // one bf16 row
+constexpr int kSlots = 4;                      // ring slots
+constexpr int kRungChunk = 2;                  // rungs per online-softmax step
+constexpr int kRowBytes = kD * 2;              // one bf16 row
 
 struct TcArgs {
   LayerTable t;
   int N;
   int tiles;
-  int slab_rows;  // 64 (mask) or 72 (interp: 65 rows used)
+  int slab_rows;   // rows of a rung slab region: 64 (mask) or 72 (interp: 65 used)
+  int slot_bytes;  // 2 * slab_rows * 128
+  int fac_stride;  // rungs per factor table (second table for interp rows lo+1)
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
@@ -180,19 +187,23 @@ __device__ __forceinline__ void load_fac(const float* f, int t, float2 (&cs)[4],
   sn[3] = make_float2(sb.z, sb.w);
 }
 
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;\n" ::"n"(kConsumers) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
+
 template <int MODE>
-__global__ void __launch_bounds__(kTcThreads, 2) fwd_tc_kernel(TcArgs a) {
+__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(TcArgs a) {
   __shared__ KeySmem ks;
-  __shared__ __align__(8) uint64_t bars[kStages + 1];  // rung stages, then the window copy
+  __shared__ __align__(8) uint64_t full_bar[kSlots];
+  __shared__ __align__(8) uint64_t empty_bar[kSlots];
   __shared__ volatile int s_err;
-  __shared__ int last_issued[kStages];  // last rung copied into each stage (-1: none)
   extern __shared__ __align__(128) unsigned char smem[];
   const int SR = a.slab_rows;
-  const int stage_bytes = 2 * SR * kRowBytes;  // K slab then V slab
-  unsigned char* stages = smem;
-  uint4* Ks = reinterpret_cast<uint4*>(smem + kStages * stage_bytes);  // K' f16, chunk ^ 4(r&1)
-  uint4* Vs = Ks + kWinRows * 8;                                          // V f16 (pi cols), chunk ^ (r&7)
-  float* fac = reinterpret_cast<float*>(Vs + kWinRows * 8);  // per rung: cos[32], sin[32] (x2 interp)
+  unsigned char* ring = smem;
+  float* fac = reinterpret_cast<float*>(smem + kSlots * a.slot_bytes);  // cos[32], sin[32] per rung
 
   const int bh = blockIdx.x / a.tiles;
   const int tile = blockIdx.x - bh * a.tiles;
@@ -208,45 +219,15 @@ __global__ void __launch_bounds__(kTcThreads, 2) fwd_tc_kernel(TcArgs a) {
   build_keys(a.t, N, &ks);
   if (tid == 0) {
     s_err = 0;
-    for (int s = 0; s < kStages; ++s) last_issued[s] = -1;
-    for (int s = 0; s <= kStages; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kTcWarps);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
   const int W = a.t.W;
   const int nr = ks.nr;
-
-  // slab of rung r: rows [first, first + SR) of K and V, copied where inside [0, N)
-  auto issue_rung = [&](int r) {
-    const int s = r % kStages;
-    if (r == 0 && a.skip_first_rung_copy) return;  // test hook: the stage never completes
-    last_issued[s] = r;
-    const int lo = ks.lo[W + r];
-    const int first = i0 - lo - (MODE == 1 ? 1 : 0);
-    const int r0 = max(first, 0);
-    const int r1 = i_last - lo + 1;  // rows read by the tile's real queries end here
-    const uint32_t bytes = r1 > r0 ? static_cast<uint32_t>(r1 - r0) * kRowBytes : 0u;
-    mbar_arrive_tx(&bars[s], 2 * bytes);
-    if (bytes) {
-      unsigned char* dst = stages + s * stage_bytes + (r0 - first) * kRowBytes;
-      bulk_g2s(dst, K + static_cast<size_t>(r0) * kD, bytes, &bars[s]);
-      bulk_g2s(dst + SR * kRowBytes, V + static_cast<size_t>(r0) * kD, bytes, &bars[s]);
-    }
-  };
-
-  // ---- copies: raw window rows into the areas of stages 2 and 3, rungs 0 and 1
-  if (tid == 0) {
-    const int w0 = max(i0 - 16, 0), w1 = i_last + 1;
-    const uint32_t bytes = static_cast<uint32_t>(w1 - w0) * kRowBytes;
-    mbar_arrive_tx(&bars[kStages], 2 * bytes);
-    bulk_g2s(stages + 2 * stage_bytes + (w0 - (i0 - 16)) * kRowBytes, K + static_cast<size_t>(w0) * kD,
-             bytes, &bars[kStages]);
-    bulk_g2s(stages + 3 * stage_bytes + (w0 - (i0 - 16)) * kRowBytes, V + static_cast<size_t>(w0) * kD,
-             bytes, &bars[kStages]);
-    for (int r = 0; r < min(nr, 2); ++r) issue_rung(r);
-  }
-
-  // ---- rung relative factors: cos / sin of lo*theta (and (lo+1)*theta for interp)
   for (int idx = tid; idx < nr * kFreq; idx += kTcThreads) {
     const int r = idx / kFreq, m = idx % kFreq;
     const int lo = ks.lo[W + r];
@@ -255,97 +236,187 @@ __global__ void __launch_bounds__(kTcThreads, 2) fwd_tc_kernel(TcArgs a) {
     fac[r * 64 + 32 + m] = e.y;
     if (MODE == 1) {
       const float2 e1 = rope_factor(a.rope_lo, a.rope_hi, lo + 1, m);
-      fac[(kMaxR + r) * 64 + m] = e1.x;
-      fac[(kMaxR + r) * 64 + 32 + m] = e1.y;
+      fac[(a.fac_stride + r) * 64 + m] = e1.x;
+      fac[(a.fac_stride + r) * 64 + 32 + m] = e1.y;
     }
   }
+  __syncthreads();  // last block-wide barrier: the roles split below
 
-  // ---- per-lane query state
   const int warp = tid >> 5, lane = tid & 31;
+  const int n_stages = 3 + nr;  // Q, window K, window V, then one per rung
+
+  // ===================================================================== producer
+  if (warp == kTcWarps) {
+    if (lane != 0) return;
+    int last_n[kSlots];
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) last_n[s] = -1;
+    const int w0 = max(i0 - 16, 0);
+    for (int n = 0; n < n_stages; ++n) {
+      if (s_err) break;
+      const int slot = n % kSlots;
+      if (!mbar_wait(&empty_bar[slot], ((n / kSlots) & 1) ^ 1, a.wait_ns)) {
+        s_err = 1;
+        break;
+      }
+      unsigned char* dst = ring + slot * a.slot_bytes;
+      if (n == 0) {  // Q rows [i0, i_last]
+        const uint32_t bytes = static_cast<uint32_t>(i_last - i0 + 1) * kRowBytes;
+        mbar_arrive_tx(&full_bar[slot], bytes);
+        bulk_g2s(dst, Q + static_cast<size_t>(i0) * kD, bytes, &full_bar[slot]);
+      } else if (n <= 2) {  // raw window rows [max(i0-16, 0), i_last] of K (n = 1) or V (n = 2)
+        const uint32_t bytes = static_cast<uint32_t>(i_last + 1 - w0) * kRowBytes;
+        mbar_arrive_tx(&full_bar[slot], bytes);
+        bulk_g2s(dst + (w0 - (i0 - 16)) * kRowBytes, (n == 1 ? K : V) + static_cast<size_t>(w0) * kD, bytes,
+                 &full_bar[slot]);
+      } else {  // rung slab: rows [first, first + SR) of K, then of V, where inside [0, N)
+        const int r = n - 3;
+        if (r == 0 && a.skip_first_rung_copy) continue;  // test hook: this stage never completes
+        const int lo = ks.lo[W + r];
+        const int first = i0 - lo - (MODE == 1 ? 1 : 0);
+        const int r0 = max(first, 0);
+        const int r1 = i_last - lo + 1;
+        const uint32_t bytes = r1 > r0 ? static_cast<uint32_t>(r1 - r0) * kRowBytes : 0u;
+        mbar_arrive_tx(&full_bar[slot], 2 * bytes);
+        if (bytes) {
+          bulk_g2s(dst + (r0 - first) * kRowBytes, K + static_cast<size_t>(r0) * kD, bytes, &full_bar[slot]);
+          bulk_g2s(dst + (SR + r0 - first) * kRowBytes, V + static_cast<size_t>(r0) * kD, bytes,
+                   &full_bar[slot]);
+        }
+      }
+      last_n[slot] = n;
+    }
+    // let every copy issued land before the CTA can exit (a completed phase returns at once)
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s)
+      if (last_n[s] >= 0) mbar_wait(&full_bar[s], (last_n[s] / kSlots) & 1, a.wait_ns);
+    if (s_err) atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
+    return;
+  }
+
+  // ===================================================================== consumers
   const int g = lane >> 2, t = lane & 3;
   const int q0 = i0 + 16 * warp;
-  int irow[2];
+  auto wait_stage = [&](int n) {
+    if (!s_err && !mbar_wait(&full_bar[n % kSlots], (n / kSlots) & 1, a.wait_ns)) {
+      s_err = 1;
+      atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
+    }
+  };
+  auto release_stage = [&](int n) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[n % kSlots]);
+  };
+
+  // ---- stage 0: Q rows -> raw q (for the rungs) and rotated f16 A fragments (window)
+  int irow[2], ic[2];
   float2 q1[2][4], q2[2][4];  // raw q * qscale: (dims 8t+2j, 8t+2j+1) and their partners
   uint32_t qa[2][2][4];       // A fragments: [row h][dim half][k-step]
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int i = q0 + g + 8 * h;
-    irow[h] = i;
-    const int ic = i < N ? i : N - 1;
-    float x[16];
-    load_part(Q + static_cast<size_t>(ic) * kD, t, x);
-#pragma unroll
-    for (int u = 0; u < 16; ++u) x[u] *= a.qscale;
-    float2 e[8];
-    abs_factors(a.rope_lo, a.rope_hi, ic, t, e);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      q1[h][j] = make_float2(x[2 * j], x[2 * j + 1]);
-      q2[h][j] = make_float2(x[8 + 2 * j], x[8 + 2 * j + 1]);
-    }
-    float y[16];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      y[u] = x[u] * e[u].x - x[8 + u] * e[u].y;
-      y[8 + u] = x[u] * e[u].y + x[8 + u] * e[u].x;
-    }
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      qa[h][0][s] = pack_h2(y[2 * s], y[2 * s + 1]);
-      qa[h][1][s] = pack_h2(y[8 + 2 * s], y[8 + 2 * s + 1]);
-    }
-  }
-
-  // ---- window rows: raw bf16 (stages 2/3 areas) -> K' f16 rotated, V f16 permuted
-  if (!mbar_wait(&bars[kStages], 0, a.wait_ns)) s_err = 1;  // (every thread waits here)
+  wait_stage(0);
   {
-    const unsigned char* kraw = stages + 2 * stage_bytes;
-    const unsigned char* vraw = stages + 3 * stage_bytes;
-    for (int task = tid; task < kWinRows * 4; task += kTcThreads) {
-      const int row = task >> 2, c = task & 3;
-      const int p = i0 - 16 + row;
-      uint4 lo4 = make_uint4(0, 0, 0, 0), hi4 = make_uint4(0, 0, 0, 0);
-      if (p >= 0 && p < N && !s_err) {
-        const uint4* r4 = reinterpret_cast<const uint4*>(kraw + row * kRowBytes);
-        const uint4 wa = r4[c], wb = r4[c + 4];
+    const unsigned char* qst = ring;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      irow[h] = q0 + g + 8 * h;
+      ic[h] = irow[h] < N ? irow[h] : N - 1;
+      const int row = ic[h] - i0;
+      float x[16];
+      if (!s_err) {
+        uint4 wa, wb;
+        lds_row_part(qst + row * kRowBytes, t, row & 1, wa, wb);
         const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w}, xb[4] = {wb.x, wb.y, wb.z, wb.w};
-        float2 e[8];
-        abs_factors(a.rope_lo, a.rope_hi, p, c, e);
-        uint32_t ya[4], yb[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float2 k1 = bf2(xa[j]), k2 = bf2(xb[j]);
-          const float2 e0 = e[2 * j], e1 = e[2 * j + 1];
-          ya[j] = pack_h2(k1.x * e0.x - k2.x * e0.y, k1.y * e1.x - k2.y * e1.y);
-          yb[j] = pack_h2(k1.x * e0.y + k2.x * e0.x, k1.y * e1.y + k2.y * e1.x);
+          x[2 * j] = bf_lo(xa[j]) * a.qscale;
+          x[2 * j + 1] = bf_hi(xa[j]) * a.qscale;
+          x[8 + 2 * j] = bf_lo(xb[j]) * a.qscale;
+          x[8 + 2 * j + 1] = bf_hi(xb[j]) * a.qscale;
         }
-        lo4 = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-        hi4 = make_uint4(yb[0], yb[1], yb[2], yb[3]);
-      }
-      const int sw = (row & 1) * 4;
-      Ks[row * 8 + (c ^ sw)] = lo4;
-      Ks[row * 8 + ((c + 4) ^ sw)] = hi4;
-    }
-    // V: dim 32h + 8t + u  ->  column 8 (4h + u/2) + 2t + (u%2)
-    for (int task = tid; task < kWinRows * 8; task += kTcThreads) {
-      const int row = task >> 3, c8 = task & 7;
-      const int p = i0 - 16 + row;
-      const int hh = c8 >> 2, tt = c8 & 3;
-      uint32_t w[4] = {0, 0, 0, 0};
-      if (p >= 0 && p < N && !s_err) {
-        const uint4 raw = reinterpret_cast<const uint4*>(vraw + row * kRowBytes)[c8];
-        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+      } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) w[j] = pack_h2(bf_lo(rw[j]), bf_hi(rw[j]));
+        for (int u = 0; u < 16; ++u) x[u] = 0.f;
       }
-      uint32_t* vrow = reinterpret_cast<uint32_t*>(Vs + row * 8);
+      float2 e[8];
+      abs_factors(a.rope_lo, a.rope_hi, ic[h], t, e);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) vrow[((4 * hh + j) ^ (row & 7)) * 4 + tt] = w[j];
+      for (int j = 0; j < 4; ++j) {
+        q1[h][j] = make_float2(x[2 * j], x[2 * j + 1]);
+        q2[h][j] = make_float2(x[8 + 2 * j], x[8 + 2 * j + 1]);
+      }
+      float y[16];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        y[u] = x[u] * e[u].x - x[8 + u] * e[u].y;
+        y[8 + u] = x[u] * e[u].y + x[8 + u] * e[u].x;
+      }
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        qa[h][0][s] = pack_h2(y[2 * s], y[2 * s + 1]);
+        qa[h][1][s] = pack_h2(y[8 + 2 * s], y[8 + 2 * s + 1]);
+      }
     }
   }
-  __syncthreads();  // Ks, Vs, fac ready; stages 2 and 3 free
-  if (tid == 0 && !s_err)
-    for (int r = 2; r < min(nr, 4); ++r) issue_rung(r);
+  release_stage(0);
+
+  // ---- stages 1, 2: window rows, converted in place: K -> K' f16 rotated (chunk c of row
+  // r at c ^ 4(r&1)), V -> f16 with columns in pi order (chunk ^ (r&7))
+  uint4* Ks = reinterpret_cast<uint4*>(ring + 1 * a.slot_bytes);
+  uint4* Vs = reinterpret_cast<uint4*>(ring + 2 * a.slot_bytes);
+  wait_stage(1);
+  for (int task = tid; task < kWinRows * 4; task += kConsumers) {
+    const int row = task >> 2, c = task & 3;
+    const int p = i0 - 16 + row;
+    uint4 lo4 = make_uint4(0, 0, 0, 0), hi4 = make_uint4(0, 0, 0, 0);
+    if (p >= 0 && p < N && !s_err) {
+      const uint4 wa = Ks[row * 8 + c], wb = Ks[row * 8 + c + 4];
+      const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w}, xb[4] = {wb.x, wb.y, wb.z, wb.w};
+      float2 e[8];
+      abs_factors(a.rope_lo, a.rope_hi, p, c, e);
+      uint32_t ya[4], yb[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 k1 = bf2(xa[j]), k2 = bf2(xb[j]);
+        const float2 e0 = e[2 * j], e1 = e[2 * j + 1];
+        ya[j] = pack_h2(k1.x * e0.x - k2.x * e0.y, k1.y * e1.x - k2.y * e1.y);
+        yb[j] = pack_h2(k1.x * e0.y + k2.x * e0.x, k1.y * e1.y + k2.y * e1.x);
+      }
+      lo4 = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+      hi4 = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+    }
+    const int sw = (row & 1) * 4;  // this thread read exactly chunks c and c+4 of this row
+    Ks[row * 8 + (c ^ sw)] = lo4;
+    Ks[row * 8 + ((c + 4) ^ sw)] = hi4;
+  }
+  wait_stage(2);
+  {
+    constexpr int kVTasks = kWinRows * 8 / kConsumers;  // 5
+    uint32_t w[kVTasks][4];
+#pragma unroll
+    for (int k = 0; k < kVTasks; ++k) {
+      const int task = tid + k * kConsumers;
+      const int row = task >> 3, c8 = task & 7;
+      const int p = i0 - 16 + row;
+      w[k][0] = w[k][1] = w[k][2] = w[k][3] = 0u;
+      if (p >= 0 && p < N && !s_err) {
+        const uint4 raw = Vs[row * 8 + c8];
+        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[k][j] = pack_h2(bf_lo(rw[j]), bf_hi(rw[j]));
+      }
+    }
+    consumer_sync();  // every raw V chunk is in registers (and K' is complete)
+#pragma unroll
+    for (int k = 0; k < kVTasks; ++k) {
+      const int task = tid + k * kConsumers;
+      const int row = task >> 3, c8 = task & 7;
+      const int hh = c8 >> 2, tt = c8 & 3;
+      uint32_t* vrow = reinterpret_cast<uint32_t*>(Vs + row * 8);
+      // dim 32hh + 8tt + u  ->  column 8 (4hh + u/2) + 2tt + (u%2)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) vrow[((4 * hh + j) ^ (row & 7)) * 4 + tt] = w[k][j];
+    }
+    consumer_sync();
+  }
 
   // ---- window: S = Q' K'^T over keys [q0-16, q0+16)
   float S[4][4];
@@ -363,6 +434,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) fwd_tc_kernel(TcArgs a) {
     for (int s = 0; s < 4; ++s)
       mma16816(S[nt], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
   }
+  release_stage(1);
   // mask: query row rr = g + 8h, key column c = 8nt + 2t + e  ->  distance rr + 16 - c
   float m[2], lw[2], lr[2];
 #pragma unroll
@@ -423,11 +495,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) fwd_tc_kernel(TcArgs a) {
       }
     }
   }
+  release_stage(2);
 
-  // ---- rungs: chunks of kRungChunk, online softmax, slabs from the stage ring
-  int ic[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) ic[h] = irow[h] < N ? irow[h] : N - 1;
+  // ---- rungs: chunks of kRungChunk, online softmax; rung r is stage 3 + r
   for (int r0 = 0; r0 < nr; r0 += kRungChunk) {
     float sc[2][kRungChunk];
 #pragma unroll
@@ -435,14 +505,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) fwd_tc_kernel(TcArgs a) {
       const int r = r0 + cc;
       const bool in = r < nr;
       const int c = W + r;
-      const int s = r % kStages;
-      if (in && !s_err && !mbar_wait(&bars[s], (r / kStages) & 1, a.wait_ns)) s_err = 1;
+      if (in) wait_stage(3 + r);
       const bool live = in && !s_err;
       const int lo = in ? ks.lo[c] : 0;
       const int need = in ? ks.need[c] : 0x7fffffff;
       const float w = (MODE == 1 && in) ? ks.w[c] : 0.f;
       const int first = i0 - lo - (MODE == 1 ? 1 : 0);
-      const unsigned char* kst = stages + s * stage_bytes;
+      const unsigned char* kst = ring + ((3 + r) % kSlots) * a.slot_bytes;
       float2 cs[4], sn[4];
       if (live) load_fac(fac + r * 64, t, cs, sn);
 #pragma unroll
@@ -456,7 +525,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) fwd_tc_kernel(TcArgs a) {
           part = rung_dot(q1[h], q2[h], cs, sn, ka, kb);
           if (MODE == 1 && w > 0.f) {
             float2 c2[4], s2[4];
-            load_fac(fac + (kMaxR + r) * 64, t, c2, s2);
+            load_fac(fac + (a.fac_stride + r) * 64, t, c2, s2);
             lds_row_part(kst + (row - 1) * kRowBytes, t, (row - 1) & 1, ka, kb);
             part = (1.f - w) * part + w * rung_dot(q1[h], q2[h], c2, s2, ka, kb);
           }
@@ -489,7 +558,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) fwd_tc_kernel(TcArgs a) {
           const float w = MODE == 1 ? ks.w[c] : 0.f;
           const int first = i0 - lo - (MODE == 1 ? 1 : 0);
           const int row = ic[h] - lo - first;
-          const unsigned char* vst = stages + (r % kStages) * stage_bytes + SR * kRowBytes;
+          const unsigned char* vst = ring + ((3 + r) % kSlots) * a.slot_bytes + SR * kRowBytes;
           uint4 va, vb;
           lds_row_part(vst + row * kRowBytes, t, row & 1, va, vb);
           const uint32_t xa[4] = {va.x, va.y, va.z, va.w}, xb[4] = {vb.x, vb.y, vb.z, vb.w};
@@ -513,23 +582,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) fwd_tc_kernel(TcArgs a) {
         }
       }
     }
-    __syncthreads();  // every warp is done with these stages
-    if (tid == 0 && !s_err)
-      for (int r = r0 + kStages; r < min(nr, r0 + kStages + kRungChunk); ++r) issue_rung(r);
+#pragma unroll
+    for (int cc = 0; cc < kRungChunk; ++cc)
+      if (r0 + cc < nr) release_stage(3 + r0 + cc);
   }
 
-  // ---- epilogue
-  if (s_err) {
-    if (tid == 0) {
-      atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
-      // only the last copy issued into a stage can still be in flight; a phase that has
-      // completed already satisfies its parity wait at once (each wait is bounded)
-      mbar_wait(&bars[kStages], 0, a.wait_ns);
-      for (int s = 0; s < kStages; ++s)
-        if (last_issued[s] >= 0) mbar_wait(&bars[s], (last_issued[s] / kStages) & 1, a.wait_ns);
-    }
-    return;
-  }
+  // ---- epilogue (nothing is written after a wait gave up; the producer reports it)
+  if (s_err) return;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     float l = lw[h];
@@ -555,11 +614,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) fwd_tc_kernel(TcArgs a) {
 
 bool tc_supported(const LayerTable& t) { return t.W <= kTcMaxW; }
 
-static size_t tc_smem_bytes(int mode, int slab_rows) {
-  return static_cast<size_t>(kStages) * 2 * slab_rows * kRowBytes + 2 * kWinRows * 8 * sizeof(uint4) +
-         static_cast<size_t>(mode == 1 ? 2 : 1) * kMaxR * 64 * sizeof(float);
-}
-
 cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k,
                           const void* v, void* o, float* lse, const float2* lo_tab,
                           const float2* hi_tab, int* status, unsigned long long wait_ns,
@@ -569,6 +623,8 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   a.N = N;
   a.tiles = (N + kTcTile - 1) / kTcTile;
   a.slab_rows = t.mode == 1 ? 72 : 64;
+  a.slot_bytes = 2 * a.slab_rows * kRowBytes;
+  a.fac_stride = t.n > 0 ? t.n : 1;  // rungs kept <= t.n (device-alpha interp may keep fewer)
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
   a.v = static_cast<const __nv_bfloat16*>(v);
@@ -582,7 +638,8 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   a.skip_first_rung_copy = skip_first_rung_copy;
   const long long blocks = static_cast<long long>(a.tiles) * B * H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const size_t smem = tc_smem_bytes(t.mode, a.slab_rows);
+  const size_t smem = static_cast<size_t>(kSlots) * a.slot_bytes +
+                      static_cast<size_t>(t.mode == 1 ? 2 : 1) * a.fac_stride * 64 * sizeof(float);
   cudaError_t e;
   if (t.mode == 0) {
     e = cudaFuncSetAttribute(fwd_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
