@@ -31,6 +31,9 @@ cudaError_t launch_bwd(const LayerTable& t, int B, int H, int N, int dtype, cons
                        const void* k, const void* v, const void* o, const float* lse,
                        const void* dO, void* dq, void* dk, void* dv, float* dalpha, void* ws,
                        const float2* lo_tab, const float2* hi_tab, cudaStream_t stream);
+cudaError_t launch_decode(const LayerTable& t, int B, int H, int N, int pos, int dtype,
+                          const void* q, const void* k, const void* v, void* o, float* lse,
+                          const float2* lo_tab, const float2* hi_tab, cudaStream_t stream);
 cudaError_t noalloc_scratch(void** out);
 size_t noalloc_scratch_bytes();
 }  // namespace fibattn
@@ -308,6 +311,26 @@ int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, c
                                      static_cast<cudaStream_t>(stream)));
   return cuda_status(launch_fwd(t, B, H, N, dtype, q, k, v, o, lse, p->d_lo, p->d_hi,
                                 static_cast<cudaStream_t>(stream)));
+}
+
+int fib_attn_decode(fib_attn_plan_t p, int layer, int B, int H, int N, int pos, int dtype,
+                    const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                    const float* alpha_dev, void* stream) {
+  int st = check_shape(p, layer, B, H, N, dtype);
+  if (st != FIB_OK) return st;
+  if (pos < 0 || pos >= N) return FIB_ERR_INVALID_ARG;
+  if (check_tensor(q) || check_tensor(k_cache) || check_tensor(v_cache) || check_tensor(o))
+    return FIB_ERR_INVALID_ARG;
+  if (o == q || o == k_cache || o == v_cache) return FIB_ERR_INVALID_ARG;
+  if (lse != nullptr && !aligned(lse, 4)) return FIB_ERR_INVALID_ARG;
+  if (alpha_dev != nullptr && !aligned(alpha_dev, 4)) return FIB_ERR_INVALID_ARG;
+  st = check_device(p);
+  if (st != FIB_OK) return st;
+  LayerTable t;
+  st = make_table(p, layer, N, p->mode == FIB_MODE_INTERP ? alpha_dev : nullptr, &t);
+  if (st != FIB_OK) return st;
+  return cuda_status(launch_decode(t, B, H, N, pos, dtype, q, k_cache, v_cache, o, lse, p->d_lo,
+                                   p->d_hi, static_cast<cudaStream_t>(stream)));
 }
 
 size_t fib_attn_bwd_workspace_size(fib_attn_plan_t p, int B, int H, int N) {

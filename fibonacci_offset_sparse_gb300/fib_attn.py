@@ -28,7 +28,7 @@ EXPORTS = [
     "fib_attn_interp_rungs", "fib_attn_plan_create", "fib_attn_plan_destroy",
     "fib_attn_plan_distances", "fib_attn_fwd", "fib_attn_bwd_workspace_size", "fib_attn_bwd",
     "fib_attn_debug_indices", "fib_attn_last_device_status", "fib_attn_plan_set_debug",
-    "fib_attn_bwd_noalloc",
+    "fib_attn_bwd_noalloc", "fib_attn_decode",
 ]
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -55,6 +55,7 @@ _SIGS = {
     "fib_attn_debug_indices": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "fib_attn_last_device_status": (_i, [_vp]),
     "fib_attn_plan_set_debug": (_i, [_vp, _i, ctypes.c_longlong]),
+    "fib_attn_decode": (_i, [_vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "fib_attn_bwd_noalloc": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                   _vp, _vp, _vp, _vp]),
 }
@@ -212,6 +213,24 @@ def fib_attn_fwd(plan: Plan, layer: int, q, k, v, o=None, lse=None, alpha_dev=No
     _check("fib_attn_fwd", lib().fib_attn_fwd(
         plan.handle, layer, B, H, N, _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
         _ptr(alpha_dev), _stream(stream)))
+    return o, lse
+
+
+def fib_attn_decode(plan: Plan, layer: int, pos: int, q, k_cache, v_cache, o=None, lse=None,
+                    alpha_dev=None, want_lse: bool = True, stream=None):
+    """One token at position pos: q [B, H, 64], caches [B, H, N, 64]; returns (o, lse)."""
+    if q.dim() != 3 or q.shape[-1] != FIB_HEAD_DIM or not q.is_cuda or not q.is_contiguous():
+        raise ValueError("q must be a contiguous CUDA [B, H, 64] tensor")
+    B, H, N = _shape(k_cache)
+    _same(k_cache, v_cache)
+    if q.shape[:2] != k_cache.shape[:2] or q.dtype != k_cache.dtype:
+        raise ValueError("q and the caches must share B, H and dtype")
+    o = torch.empty_like(q) if o is None else o
+    if lse is None and want_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    _check("fib_attn_decode", lib().fib_attn_decode(
+        plan.handle, layer, B, H, N, pos, _DT[q.dtype], _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(o), _ptr(lse), _ptr(alpha_dev), _stream(stream)))
     return o, lse
 
 

@@ -133,6 +133,19 @@ int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
                  const void* q, const void* k, const void* v, void* o, float* lse,
                  const float* alpha_dev, void* stream);
 
+/* ------------------------------------------------------------------------ decode ----
+ * One new token per (b, h) against a KV cache (Key results 2, "Efficiency": inference
+ * latency of the mask and the interpolated path).  The token sits at position pos of a
+ * sequence of length N (0 <= pos < N <= N_max) and attends exactly what row pos of
+ * fib_attn_fwd at length N attends (N matters for the power-of-two base only).
+ * q: [B, H, 64] raw (unrotated) query; k_cache, v_cache: [B, H, N, 64] raw rows, of which
+ * rows 0..pos are read; o: [B, H, 64]; lse: [B, H] float32 or NULL.  Dtype and alpha_dev
+ * as fib_attn_fwd.  Errors as fib_attn_fwd, plus FIB_ERR_INVALID_ARG for pos outside
+ * [0, N).                                                                              */
+int fib_attn_decode(fib_attn_plan_t p, int layer, int B, int H, int N, int pos, int dtype,
+                    const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                    const float* alpha_dev, void* stream);
+
 /* --------------------------------------------------------------------- backward ----
  * Gradients of l = sum(O * dO) for one layer, given the forward's o and lse.
  * dq, dk, dv: [B, H, N, 64] device (dtype of the inputs), fully written.
