@@ -126,20 +126,6 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* smem
                : "r"(smem_addr(smem_row)));
 }
 
-// e^{i p theta_m} for m = 8t .. 8t+7 at absolute position p.
-__device__ __forceinline__ void abs_factors(const float2* __restrict__ lo_tab,
-                                            const float2* __restrict__ hi_tab, int p, int t,
-                                            float2 (&e)[8]) {
-  const float4* h4 = reinterpret_cast<const float4*>(hi_tab + (p >> 6) * kFreq + 8 * t);
-  const float4* l4 = reinterpret_cast<const float4*>(lo_tab + (p & 63) * kFreq + 8 * t);
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const float4 a = __ldg(h4 + u), b = __ldg(l4 + u);
-    e[2 * u] = make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
-    e[2 * u + 1] = make_float2(a.z * b.z - a.w * b.w, a.z * b.w + a.w * b.z);
-  }
-}
-
 // Read the 16 dims D_t of a 128-byte bf16 row in shared memory as two 16-byte words;
 // odd rows read their halves in the opposite order, so the 8 lanes of a phase (two rows
 // x four t) hit 8 distinct bank groups.
@@ -225,22 +211,9 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  __syncthreads();
+  __syncthreads();  // the only block-wide barrier: the roles split below
   const int W = a.t.W;
   const int nr = ks.nr;
-  for (int idx = tid; idx < nr * kFreq; idx += kTcThreads) {
-    const int r = idx / kFreq, m = idx % kFreq;
-    const int lo = ks.lo[W + r];
-    const float2 e = rope_factor(a.rope_lo, a.rope_hi, lo, m);
-    fac[r * 64 + m] = e.x;
-    fac[r * 64 + 32 + m] = e.y;
-    if (MODE == 1) {
-      const float2 e1 = rope_factor(a.rope_lo, a.rope_hi, lo + 1, m);
-      fac[(a.fac_stride + r) * 64 + m] = e1.x;
-      fac[(a.fac_stride + r) * 64 + 32 + m] = e1.y;
-    }
-  }
-  __syncthreads();  // last block-wide barrier: the roles split below
 
   const int warp = tid >> 5, lane = tid & 31;
   const int n_stages = 3 + nr;  // Q, window K, window V, then one per rung
@@ -297,6 +270,57 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
   // ===================================================================== consumers
   const int g = lane >> 2, t = lane & 3;
   const int q0 = i0 + 16 * warp;
+  // Every factor load is issued here, before the first stage wait, so that its latency
+  // overlaps the first copies.  (1) rung factors e^{i lo theta} into shared memory;
+  for (int idx = tid; idx < nr * kFreq; idx += kConsumers) {
+    const int r = idx / kFreq, m = idx % kFreq;
+    const int lo = ks.lo[W + r];
+    const float2 e = rope_factor(a.rope_lo, a.rope_hi, lo, m);
+    fac[r * 64 + m] = e.x;
+    fac[r * 64 + 32 + m] = e.y;
+    if (MODE == 1) {
+      const float2 e1 = rope_factor(a.rope_lo, a.rope_hi, lo + 1, m);
+      fac[(a.fac_stride + r) * 64 + m] = e1.x;
+      fac[(a.fac_stride + r) * 64 + 32 + m] = e1.y;
+    }
+  }
+  // (2) window rotation factors.  Q' and K' are rotated by their offset from the tile base
+  // p0 = i0 - 16 instead of their absolute position: the common e^{i p0 theta} cancels in
+  // q'_i . k'_j, and the offsets (< 80) need only the small lo table (plus hi row 1).
+  // Rows of this thread: Q rows g, g+8 of the warp (offsets 16 + 16 warp + g (+8)) and the
+  // K' conversion tasks (row tid/4 + 32k, frequencies 8t..8t+7 since tid % 4 == t).
+  float2 eq[2][8], ek[3][8];
+  {
+    float2 h1[8];  // e^{i 64 theta_m}
+    const float4* h4 = reinterpret_cast<const float4*>(a.rope_hi + kFreq + 8 * t);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 x = __ldg(h4 + u);
+      h1[2 * u] = make_float2(x.x, x.y);
+      h1[2 * u + 1] = make_float2(x.z, x.w);
+    }
+    auto rel = [&](int off, float2 (&e)[8]) {
+      const int o = off < kWinRows ? off : 0;
+      const float4* l4 = reinterpret_cast<const float4*>(a.rope_lo + (o & 63) * kFreq + 8 * t);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 x = __ldg(l4 + u);
+        e[2 * u] = make_float2(x.x, x.y);
+        e[2 * u + 1] = make_float2(x.z, x.w);
+      }
+      if (o >= 64) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float2 b = e[u];
+          e[u] = make_float2(h1[u].x * b.x - h1[u].y * b.y, h1[u].x * b.y + h1[u].y * b.x);
+        }
+      }
+    };
+#pragma unroll
+    for (int h = 0; h < 2; ++h) rel(16 + 16 * warp + g + 8 * h, eq[h]);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) rel((tid >> 2) + 32 * k, ek[k]);
+  }
   auto wait_stage = [&](int n) {
     if (!s_err && !mbar_wait(&full_bar[n % kSlots], (n / kSlots) & 1, a.wait_ns)) {
       s_err = 1;
@@ -336,8 +360,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
 #pragma unroll
         for (int u = 0; u < 16; ++u) x[u] = 0.f;
       }
-      float2 e[8];
-      abs_factors(a.rope_lo, a.rope_hi, ic[h], t, e);
+      const float2(&e)[8] = eq[h];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         q1[h][j] = make_float2(x[2 * j], x[2 * j + 1]);
@@ -363,15 +386,17 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
   uint4* Ks = reinterpret_cast<uint4*>(ring + 1 * a.slot_bytes);
   uint4* Vs = reinterpret_cast<uint4*>(ring + 2 * a.slot_bytes);
   wait_stage(1);
-  for (int task = tid; task < kWinRows * 4; task += kConsumers) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const int task = tid + k * kConsumers;
+    if (task >= kWinRows * 4) break;
     const int row = task >> 2, c = task & 3;
     const int p = i0 - 16 + row;
     uint4 lo4 = make_uint4(0, 0, 0, 0), hi4 = make_uint4(0, 0, 0, 0);
     if (p >= 0 && p < N && !s_err) {
       const uint4 wa = Ks[row * 8 + c], wb = Ks[row * 8 + c + 4];
       const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w}, xb[4] = {wb.x, wb.y, wb.z, wb.w};
-      float2 e[8];
-      abs_factors(a.rope_lo, a.rope_hi, p, c, e);
+      const float2(&e)[8] = ek[k];
       uint32_t ya[4], yb[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
