@@ -34,7 +34,7 @@ def test_decode_equals_forward_row(dtype, mode, alpha, kind, W, N):
     base = oracle.fibonacci_base() if kind == "fib" else oracle.pow2_base(N)
     O_ref, lse_ref = oracle.attend(inputs.as_f64(q), inputs.as_f64(k), inputs.as_f64(v), alpha, base, W, mode)
     tol = 1e-5 if dtype == "f32" else 1e-2
-    for pos in (0, 1, W - 1, W, 377, N // 2, N - 1):
+    for pos in sorted({p for p in (0, 1, W - 1, W, 377, N // 2, N - 1) if p < N}):
         o, lse = fa.fib_attn_decode(plan, 0, pos, q[:, :, pos].contiguous().cuda(), kc, vc)
         torch.cuda.synchronize()
         ref = O_ref[:, :, pos]
