@@ -145,19 +145,19 @@ __device__ __forceinline__ void lds_row_part(const unsigned char* row, int t, bo
 // z = q e^{i d theta} (cs = cos, sn = sin of d theta for the lane's frequencies).
 __device__ __forceinline__ float rung_dot(const float2 (&q1)[4], const float2 (&q2)[4],
                                           const float2 (&cs)[4], const float2 (&sn)[4],
-                                          const uint4& ka, const uint4& kb) {
+                                          const float2 (&ns)[4], const uint4& ka, const uint4& kb) {
   const uint32_t xa[4] = {ka.x, ka.y, ka.z, ka.w}, xb[4] = {kb.x, kb.y, kb.z, kb.w};
-  float2 acc = make_float2(0.f, 0.f);
+  float2 acc1 = make_float2(0.f, 0.f), acc2 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const float2 k1 = bf2(xa[j]), k2 = bf2(xb[j]);
-    const float2 nq2 = make_float2(-q2[j].x, -q2[j].y);
-    const float2 z1 = __ffma2_rn(cs[j], q1[j], __fmul2_rn(sn[j], nq2));
-    const float2 z2 = __ffma2_rn(sn[j], q1[j], __fmul2_rn(cs[j], q2[j]));
-    acc = __ffma2_rn(z1, k1, acc);
-    acc = __ffma2_rn(z2, k2, acc);
+    // z = q e^{i d theta}: z1 = c q1 - s q2, z2 = s q1 + c q2
+    const float2 z1 = __ffma2_rn(ns[j], q2[j], __fmul2_rn(cs[j], q1[j]));
+    const float2 z2 = __ffma2_rn(cs[j], q2[j], __fmul2_rn(sn[j], q1[j]));
+    acc1 = __ffma2_rn(z1, k1, acc1);
+    acc2 = __ffma2_rn(z2, k2, acc2);
   }
-  return acc.x + acc.y;
+  return (acc1.x + acc2.x) + (acc1.y + acc2.y);
 }
 
 __device__ __forceinline__ void load_fac(const float* f, int t, float2 (&cs)[4], float2 (&sn)[4]) {
@@ -522,42 +522,74 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
   }
   release_stage(2);
 
-  // ---- rungs: chunks of kRungChunk, online softmax; rung r is stage 3 + r
+  // ---- rungs: chunks of kRungChunk, online softmax; rung r is stage 3 + r.
+  // The slab row of query i is i - i0 (+1 for interp) for every rung.  Inside a warp the
+  // arithmetic is branch-free: a row that does not attend the rung reads the slab's first
+  // copied row instead (finite data) and gets p = 0; a warp none of whose rows attends the
+  // rung skips it as a whole (a uniform branch).
+  int srow[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) srow[h] = ic[h] - i0 + (MODE == 1 ? 1 : 0);
   for (int r0 = 0; r0 < nr; r0 += kRungChunk) {
+#pragma unroll
+    for (int cc = 0; cc < kRungChunk; ++cc)
+      if (r0 + cc < nr) wait_stage(3 + r0 + cc);
     float sc[2][kRungChunk];
+    bool act[kRungChunk];
+    int rowu[2][kRungChunk], fcop[kRungChunk];
 #pragma unroll
     for (int cc = 0; cc < kRungChunk; ++cc) {
-      const int r = r0 + cc;
-      const bool in = r < nr;
+      const int r = r0 + cc < nr ? r0 + cc : r0;
       const int c = W + r;
-      if (in) wait_stage(3 + r);
-      const bool live = in && !s_err;
-      const int lo = in ? ks.lo[c] : 0;
-      const int need = in ? ks.need[c] : 0x7fffffff;
-      const float w = (MODE == 1 && in) ? ks.w[c] : 0.f;
-      const int first = i0 - lo - (MODE == 1 ? 1 : 0);
-      const unsigned char* kst = ring + ((3 + r) % kSlots) * a.slot_bytes;
-      float2 cs[4], sn[4];
-      if (live) load_fac(fac + r * 64, t, cs, sn);
+      const int lo = ks.lo[c];
+      const bool in = (r0 + cc < nr) && !s_err;
+      bool ok[2];
+      // first copied row of this slab (slab rows start at global row i0 - lo - interp)
+      const int first_copied = max(0, lo - i0 + (MODE == 1 ? 1 : 0));
+      fcop[cc] = first_copied;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const bool ok = live && ic[h] >= need;
-        float part = 0.f;
-        if (ok) {
-          const int row = ic[h] - lo - first;
+        ok[h] = in && ic[h] >= ks.need[c];
+        rowu[h][cc] = ok[h] ? srow[h] : first_copied;
+      }
+      act[cc] = __any_sync(0xffffffffu, ok[0] || ok[1]);
+      sc[0][cc] = sc[1][cc] = -INFINITY;
+      if (act[cc]) {
+        const unsigned char* kst = ring + ((3 + r) % kSlots) * a.slot_bytes;
+        float2 cs[4], sn[4], ns[4];
+        load_fac(fac + r * 64, t, cs, sn);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ns[j] = make_float2(-sn[j].x, -sn[j].y);
+        float part[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int row = rowu[h][cc];
           uint4 ka, kb;
           lds_row_part(kst + row * kRowBytes, t, row & 1, ka, kb);
-          part = rung_dot(q1[h], q2[h], cs, sn, ka, kb);
-          if (MODE == 1 && w > 0.f) {
-            float2 c2[4], s2[4];
+          part[h] = rung_dot(q1[h], q2[h], cs, sn, ns, ka, kb);
+        }
+        if (MODE == 1) {
+          const float w = ks.w[c];
+          if (w > 0.f) {  // uniform: w belongs to the rung
+            float2 c2[4], s2[4], n2[4];
             load_fac(fac + (a.fac_stride + r) * 64, t, c2, s2);
-            lds_row_part(kst + (row - 1) * kRowBytes, t, (row - 1) & 1, ka, kb);
-            part = (1.f - w) * part + w * rung_dot(q1[h], q2[h], c2, s2, ka, kb);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) n2[j] = make_float2(-s2[j].x, -s2[j].y);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int row = max(rowu[h][cc] - 1, first_copied);
+              uint4 ka, kb;
+              lds_row_part(kst + row * kRowBytes, t, row & 1, ka, kb);
+              part[h] = (1.f - w) * part[h] + w * rung_dot(q1[h], q2[h], c2, s2, n2, ka, kb);
+            }
           }
         }
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        sc[h][cc] = ok ? part : -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          part[h] += __shfl_xor_sync(0xffffffffu, part[h], 1);
+          part[h] += __shfl_xor_sync(0xffffffffu, part[h], 2);
+          sc[h][cc] = ok[h] ? part[h] : -INFINITY;
+        }
       }
     }
 #pragma unroll
@@ -572,37 +604,37 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
       const float2 corr2 = make_float2(corr, corr);
 #pragma unroll
       for (int nd = 0; nd < 8; ++nd) O[nd][h] = __fmul2_rn(O[nd][h], corr2);
+    }
 #pragma unroll
-      for (int cc = 0; cc < kRungChunk; ++cc) {
-        const float p = exp2f(sc[h][cc] - mc);
+    for (int cc = 0; cc < kRungChunk; ++cc) {
+      if (!act[cc]) continue;  // uniform
+      const int r = r0 + cc;
+      const float w = MODE == 1 ? ks.w[W + r] : 0.f;
+      const unsigned char* vst = ring + ((3 + r) % kSlots) * a.slot_bytes + SR * kRowBytes;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float p = exp2f(sc[h][cc] - m[h]);  // 0 for a row that does not attend
         lr[h] += p;
-        if (p > 0.f) {
-          const int r = r0 + cc;
-          const int c = W + r;
-          const int lo = ks.lo[c];
-          const float w = MODE == 1 ? ks.w[c] : 0.f;
-          const int first = i0 - lo - (MODE == 1 ? 1 : 0);
-          const int row = ic[h] - lo - first;
-          const unsigned char* vst = ring + ((3 + r) % kSlots) * a.slot_bytes + SR * kRowBytes;
-          uint4 va, vb;
-          lds_row_part(vst + row * kRowBytes, t, row & 1, va, vb);
-          const uint32_t xa[4] = {va.x, va.y, va.z, va.w}, xb[4] = {vb.x, vb.y, vb.z, vb.w};
-          const float p0 = p * (1.f - w);
-          const float2 pp = make_float2(p0, p0);
+        const int row = rowu[h][cc];
+        uint4 va, vb;
+        lds_row_part(vst + row * kRowBytes, t, row & 1, va, vb);
+        const uint32_t xa[4] = {va.x, va.y, va.z, va.w}, xb[4] = {vb.x, vb.y, vb.z, vb.w};
+        const float p0 = p * (1.f - w);
+        const float2 pp = make_float2(p0, p0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          O[j][h] = __ffma2_rn(pp, bf2(xa[j]), O[j][h]);
+          O[4 + j][h] = __ffma2_rn(pp, bf2(xb[j]), O[4 + j][h]);
+        }
+        if (MODE == 1 && w > 0.f) {
+          const int row1 = max(row - 1, fcop[cc]);
+          lds_row_part(vst + row1 * kRowBytes, t, row1 & 1, va, vb);
+          const uint32_t ya[4] = {va.x, va.y, va.z, va.w}, yb[4] = {vb.x, vb.y, vb.z, vb.w};
+          const float2 pw = make_float2(p * w, p * w);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            O[j][h] = __ffma2_rn(pp, bf2(xa[j]), O[j][h]);
-            O[4 + j][h] = __ffma2_rn(pp, bf2(xb[j]), O[4 + j][h]);
-          }
-          if (MODE == 1 && w > 0.f) {
-            lds_row_part(vst + (row - 1) * kRowBytes, t, (row - 1) & 1, va, vb);
-            const uint32_t ya[4] = {va.x, va.y, va.z, va.w}, yb[4] = {vb.x, vb.y, vb.z, vb.w};
-            const float2 pw = make_float2(p * w, p * w);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              O[j][h] = __ffma2_rn(pw, bf2(ya[j]), O[j][h]);
-              O[4 + j][h] = __ffma2_rn(pw, bf2(yb[j]), O[4 + j][h]);
-            }
+            O[j][h] = __ffma2_rn(pw, bf2(ya[j]), O[j][h]);
+            O[4 + j][h] = __ffma2_rn(pw, bf2(yb[j]), O[4 + j][h]);
           }
         }
       }
