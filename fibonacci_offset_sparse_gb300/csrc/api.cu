@@ -7,7 +7,10 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
+#include <utility>
 #include <set>
 #include <vector>
 
@@ -23,7 +26,7 @@ bool tc_supported(const LayerTable& t);
 cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k,
                           const void* v, void* o, float* lse, const float2* lo_tab,
                           const float2* hi_tab, int* status, unsigned long long wait_ns,
-                          int skip_first_rung_copy, cudaStream_t stream);
+                          int skip_first_rung_copy, const float* host_fac, cudaStream_t stream);
 cudaError_t launch_debug_indices(const LayerTable& t, int N, int i0, int i1, int32_t* out,
                                  float* w_out, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int H, int N);
@@ -52,6 +55,9 @@ struct fib_attn_plan_s {
   int* d_status = nullptr;
   unsigned long long wait_ns = 1000000000ULL;  // bound of every device-side wait (1 s)
   int skip_first_rung_copy = 0;                // test hook, see fib_attn_plan_set_debug
+  // rung RoPE factors per (layer, N): cos/sin(lo theta_m) (+ (lo+1) theta_m), binary64-built
+  std::map<std::pair<int, int>, std::vector<float>> fac_cache;
+  std::mutex fac_mu;
 };
 
 namespace {
@@ -96,6 +102,26 @@ int make_table(const fib_attn_plan_s* p, int layer, int N, const float* alpha_de
     t->alpha_dev = alpha_dev;
   }
   return FIB_OK;
+}
+
+// cos / sin of (lo theta_m) and ((lo+1) theta_m) for the layer's host-side rungs, in the
+// layout of the tensor-core forward's factor parameter (2 tables x kMaxR rungs x 64).
+const float* rung_factors(fib_attn_plan_s* p, int layer, int N, const LayerTable& t) {
+  std::lock_guard<std::mutex> lock(p->fac_mu);
+  auto key = std::make_pair(layer, N);
+  auto it = p->fac_cache.find(key);
+  if (it != p->fac_cache.end()) return it->second.data();
+  std::vector<float> f(2 * kMaxR * 64, 0.f);
+  for (int r = 0; r < t.n; ++r)
+    for (int m = 0; m < kFreq; ++m) {
+      const double theta = std::pow(p->rope_base, -2.0 * m / kD);
+      for (int tab = 0; tab < 2; ++tab) {
+        const double ang = static_cast<double>(t.lo[r] + tab) * theta;
+        f[(tab * kMaxR + r) * 64 + m] = static_cast<float>(std::cos(ang));
+        f[(tab * kMaxR + r) * 64 + 32 + m] = static_cast<float>(std::sin(ang));
+      }
+    }
+  return p->fac_cache.emplace(key, std::move(f)).first->second.data();
 }
 
 int check_device(const fib_attn_plan_s* p) {
@@ -308,6 +334,7 @@ int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, c
   if (dtype == FIB_DTYPE_BF16 && tc_supported(t))
     return cuda_status(launch_fwd_tc(t, B, H, N, q, k, v, o, lse, p->d_lo, p->d_hi, p->d_status,
                                      p->wait_ns, p->skip_first_rung_copy,
+                                     t.alpha_dev == nullptr ? rung_factors(p, layer, N, t) : nullptr,
                                      static_cast<cudaStream_t>(stream)));
   return cuda_status(launch_fwd(t, B, H, N, dtype, q, k, v, o, lse, p->d_lo, p->d_hi,
                                 static_cast<cudaStream_t>(stream)));

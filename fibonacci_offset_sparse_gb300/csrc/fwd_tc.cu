@@ -61,6 +61,14 @@ struct TcArgs {
   int* status;                 // plan status word (FIB_ERR_TIMEOUT on a wait that gave up)
   unsigned long long wait_ns;  // bound of every mbarrier wait
   int skip_first_rung_copy;    // test hook: never arrive on rung 0's stage
+  int host_fac;                // rung factors come precomputed in TcFac (else computed here)
+};
+
+// Rung factors cos / sin of (lo theta_m) (and of (lo+1) theta_m for interp rows), built in
+// binary64 on the host, passed by value: table 0 at v[r*64 + {0..31: cos, 32..63: sin}],
+// table 1 at v[(kMaxR + r)*64 + ...].
+struct TcFac {
+  float v[2 * kMaxR * 64];
 };
 
 // ------------------------------------------------------------------ small PTX helpers
@@ -181,7 +189,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(TcArgs a) {
+__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(TcArgs a, const __grid_constant__ TcFac pf) {
   __shared__ KeySmem ks;
   __shared__ __align__(8) uint64_t full_bar[kSlots];
   __shared__ __align__(8) uint64_t empty_bar[kSlots];
@@ -271,8 +279,15 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
   const int g = lane >> 2, t = lane & 3;
   const int q0 = i0 + 16 * warp;
   // Every factor load is issued here, before the first stage wait, so that its latency
-  // overlaps the first copies.  (1) rung factors e^{i lo theta} into shared memory;
-  for (int idx = tid; idx < nr * kFreq; idx += kConsumers) {
+  // overlaps the first copies.  (1) rung factors e^{i lo theta} into shared memory, from the
+  // kernel parameters when the host built them, else from the RoPE tables;
+  if (a.host_fac) {
+    for (int idx = tid; idx < nr * 64; idx += kConsumers) {
+      fac[idx] = pf.v[idx];
+      if (MODE == 1) fac[a.fac_stride * 64 + idx] = pf.v[kMaxR * 64 + idx];
+    }
+  }
+  for (int idx = a.host_fac ? nr * kFreq : tid; idx < nr * kFreq; idx += kConsumers) {
     const int r = idx / kFreq, m = idx % kFreq;
     const int lo = ks.lo[W + r];
     const float2 e = rope_factor(a.rope_lo, a.rope_hi, lo, m);
@@ -674,8 +689,12 @@ bool tc_supported(const LayerTable& t) { return t.W <= kTcMaxW; }
 cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k,
                           const void* v, void* o, float* lse, const float2* lo_tab,
                           const float2* hi_tab, int* status, unsigned long long wait_ns,
-                          int skip_first_rung_copy, cudaStream_t stream) {
+                          int skip_first_rung_copy, const float* host_fac, cudaStream_t stream) {
   TcArgs a;
+  TcFac f;
+  a.host_fac = host_fac != nullptr;
+  if (host_fac != nullptr)
+    for (int i = 0; i < 2 * kMaxR * 64; ++i) f.v[i] = host_fac[i];
   a.t = t;
   a.N = N;
   a.tiles = (N + kTcTile - 1) / kTcTile;
@@ -701,11 +720,11 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   if (t.mode == 0) {
     e = cudaFuncSetAttribute(fwd_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    fwd_tc_kernel<0><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a);
+    fwd_tc_kernel<0><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a, f);
   } else {
     e = cudaFuncSetAttribute(fwd_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    fwd_tc_kernel<1><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a);
+    fwd_tc_kernel<1><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a, f);
   }
   return cudaGetLastError();
 }
