@@ -61,14 +61,10 @@ struct TcArgs {
   int* status;                 // plan status word (FIB_ERR_TIMEOUT on a wait that gave up)
   unsigned long long wait_ns;  // bound of every mbarrier wait
   int skip_first_rung_copy;    // test hook: never arrive on rung 0's stage
-  int host_fac;                // rung factors come precomputed in TcFac (else computed here)
-};
-
-// Rung factors cos / sin of (lo theta_m) (and of (lo+1) theta_m for interp rows), built in
-// binary64 on the host, passed by value: table 0 at v[r*64 + {0..31: cos, 32..63: sin}],
-// table 1 at v[(kMaxR + r)*64 + ...].
-struct TcFac {
-  float v[2 * kMaxR * 64];
+  // Rung factors cos / sin of (lo theta_m) and, for interp, of ((lo+1) theta_m), built in
+  // binary64 by the plan: table 0 at fac_dev[r*64 + {0..31: cos, 32..63: sin}], table 1 at
+  // fac_dev[(kMaxR + r)*64 + ...].  Null: computed here from the RoPE tables.
+  const float* fac_dev;
 };
 
 // ------------------------------------------------------------------ small PTX helpers
@@ -189,7 +185,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(TcArgs a, const __grid_constant__ TcFac pf) {
+__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(TcArgs a) {
   __shared__ KeySmem ks;
   __shared__ __align__(8) uint64_t full_bar[kSlots];
   __shared__ __align__(8) uint64_t empty_bar[kSlots];
@@ -241,10 +237,16 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
         break;
       }
       unsigned char* dst = ring + slot * a.slot_bytes;
-      if (n == 0) {  // Q rows [i0, i_last]
+      if (n == 0) {  // Q rows [i0, i_last]; then the plan's rung factor tables, if any
         const uint32_t bytes = static_cast<uint32_t>(i_last - i0 + 1) * kRowBytes;
-        mbar_arrive_tx(&full_bar[slot], bytes);
+        const uint32_t fbytes = a.fac_dev != nullptr ? static_cast<uint32_t>(nr) * 256u : 0u;
+        mbar_arrive_tx(&full_bar[slot], bytes + (MODE == 1 ? 2 : 1) * fbytes);
         bulk_g2s(dst, Q + static_cast<size_t>(i0) * kD, bytes, &full_bar[slot]);
+        if (fbytes) {
+          bulk_g2s(dst + kTcTile * kRowBytes, a.fac_dev, fbytes, &full_bar[slot]);
+          if (MODE == 1)  // table 1 packed right after table 0
+            bulk_g2s(dst + kTcTile * kRowBytes + fbytes, a.fac_dev + kMaxR * 64, fbytes, &full_bar[slot]);
+        }
       } else if (n <= 2) {  // raw window rows [max(i0-16, 0), i_last] of K (n = 1) or V (n = 2)
         const uint32_t bytes = static_cast<uint32_t>(i_last + 1 - w0) * kRowBytes;
         mbar_arrive_tx(&full_bar[slot], bytes);
@@ -281,13 +283,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
   // Every factor load is issued here, before the first stage wait, so that its latency
   // overlaps the first copies.  (1) rung factors e^{i lo theta} into shared memory, from the
   // kernel parameters when the host built them, else from the RoPE tables;
-  if (a.host_fac) {
-    for (int idx = tid; idx < nr * 64; idx += kConsumers) {
-      fac[idx] = pf.v[idx];
-      if (MODE == 1) fac[a.fac_stride * 64 + idx] = pf.v[kMaxR * 64 + idx];
-    }
-  }
-  for (int idx = a.host_fac ? nr * kFreq : tid; idx < nr * kFreq; idx += kConsumers) {
+  for (int idx = a.fac_dev != nullptr ? nr * kFreq : tid; idx < nr * kFreq; idx += kConsumers) {
     const int r = idx / kFreq, m = idx % kFreq;
     const int lo = ks.lo[W + r];
     const float2 e = rope_factor(a.rope_lo, a.rope_hi, lo, m);
@@ -392,6 +388,13 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
         qa[h][0][s] = pack_h2(y[2 * s], y[2 * s + 1]);
         qa[h][1][s] = pack_h2(y[8 + 2 * s], y[8 + 2 * s + 1]);
       }
+    }
+  }
+  if (a.fac_dev != nullptr) {  // the factor tables rode in after the Q rows
+    const float* src = reinterpret_cast<const float*>(ring + kTcTile * kRowBytes);
+    for (int idx = tid; idx < nr * 64; idx += kConsumers) {
+      fac[idx] = src[idx];
+      if (MODE == 1) fac[a.fac_stride * 64 + idx] = src[nr * 64 + idx];
     }
   }
   release_stage(0);
@@ -689,12 +692,12 @@ bool tc_supported(const LayerTable& t) { return t.W <= kTcMaxW; }
 cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k,
                           const void* v, void* o, float* lse, const float2* lo_tab,
                           const float2* hi_tab, int* status, unsigned long long wait_ns,
-                          int skip_first_rung_copy, const float* host_fac, cudaStream_t stream) {
+                          int skip_first_rung_copy, const float* fac_dev, cudaStream_t stream) {
   TcArgs a;
-  TcFac f;
-  a.host_fac = host_fac != nullptr;
-  if (host_fac != nullptr)
-    for (int i = 0; i < 2 * kMaxR * 64; ++i) f.v[i] = host_fac[i];
+  // the Q rows (8 KB) and the factor tables (256 B per rung, two tables for interp) share a slot
+  const int slot = 2 * (t.mode == 1 ? 72 : 64) * kRowBytes;
+  const bool fits = kTcTile * kRowBytes + (t.mode == 1 ? 2 : 1) * t.n * 256 <= slot;
+  a.fac_dev = fits ? fac_dev : nullptr;
   a.t = t;
   a.N = N;
   a.tiles = (N + kTcTile - 1) / kTcTile;
@@ -720,11 +723,11 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   if (t.mode == 0) {
     e = cudaFuncSetAttribute(fwd_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    fwd_tc_kernel<0><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a, f);
+    fwd_tc_kernel<0><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a);
   } else {
     e = cudaFuncSetAttribute(fwd_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    fwd_tc_kernel<1><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a, f);
+    fwd_tc_kernel<1><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a);
   }
   return cudaGetLastError();
 }
