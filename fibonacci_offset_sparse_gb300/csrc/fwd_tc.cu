@@ -101,6 +101,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     if (global_ns() - t0 > limit_ns) return false;
   }
 }
+// The producer's wait: like mbar_wait, but it backs off with __nanosleep between polls so
+// that a waiting producer leaves the issue slots to the consumer warps of its SM.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  unsigned sleep_ns = 32;
+  while (true) {
+    __nanosleep(sleep_ns);
+    if (mbar_try(bar, parity)) return true;
+    if (sleep_ns < 512) sleep_ns *= 2;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
@@ -232,7 +245,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
     for (int n = 0; n < n_stages; ++n) {
       if (s_err) break;
       const int slot = n % kSlots;
-      if (!mbar_wait(&empty_bar[slot], ((n / kSlots) & 1) ^ 1, a.wait_ns)) {
+      if (!mbar_wait_backoff(&empty_bar[slot], ((n / kSlots) & 1) ^ 1, a.wait_ns)) {
         s_err = 1;
         break;
       }
