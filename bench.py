@@ -241,16 +241,36 @@ def time_device(w, steps, warmup, device, rank, world):
     return res
 
 
+def time_dense_sdpa(w, device, reps=20):
+    """Dense causal attention on the same shape through PyTorch's fused attention (a library
+    kernel, timed only as the dense comparison point): milliseconds per layer."""
+    import torch
+    from fibonacci_offset_sparse_gb300 import inputs
+    q, k, v = (t.to(device) for t in inputs.qkv(w["B"], w["H"], w["N"], 64, w["cfg"], 0, w["dtype"]))
+    f = torch.nn.functional.scaled_dot_product_attention
+    for _ in range(3):
+        f(q, k, v, is_causal=True)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        f(q, k, v, is_causal=True)
+    e1.record()
+    torch.cuda.synchronize(device)
+    return e0.elapsed_time(e1) / reps
+
+
 # ----------------------------------------------------------------------------- CPU oracle
-def time_oracle(w, n_layers_sample, rank_layers=None):
-    """Oracle seconds per layer of the workload on a sample of layers (and, for long
-    sequences, of heads); returns (seconds per full layer, sample description)."""
+def time_oracle(w, n_layers_sample, heads=None):
+    """Oracle seconds per layer of the workload on a sample of layers and heads (every batch
+    row, the full sequence); returns (seconds per full layer, sample description)."""
     import numpy as np  # noqa: F401
     import oracle
     from fibonacci_offset_sparse_gb300 import inputs
     alphas = alphas_for(w)
     base = (lambda N: oracle.fibonacci_base()) if w["base"] == "fib" else oracle.pow2_base
-    heads = w["H"] if w["N"] <= 4096 else 1
+    if heads is None:
+        heads = w["H"] if w["N"] <= 4096 else 1
     layers = list(range(min(n_layers_sample, w["L"])))
     t_total = 0.0
     for l in layers:
@@ -293,13 +313,13 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        per_layer, desc = time_oracle(w, 1)  # warm/size
-        vals = []
+        sample_heads = min(2, w["H"])
         for _ in range(args.warmup):
-            pass
+            time_oracle(w, 1, sample_heads)
+        vals = []
         t0 = time.perf_counter()
         for s in range(args.steps):
-            pl, desc = time_oracle(w, 1)
+            pl, desc = time_oracle(w, 1, sample_heads)
             vals.append(pl)
         el = time.perf_counter() - t0
         per_layer = statistics.mean(vals)
@@ -346,7 +366,7 @@ def main():
                      "algorithmic_bytes_per_launch": algo,
                      "avg_launch_us": launch_s * 1e6},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
-                "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"]},
+                "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"], "gpu_launches": r["e2e_launches"]},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
@@ -360,9 +380,18 @@ def main():
             sec[name] = {"value": ws["B"] * ws["N"] * world / (rs["ms_per_step"] / 1e3), "unit": UNIT,
                          "ms_per_step": rs["ms_per_step"], "avg_launch_us": ls * 1e6,
                          "achieved_gbs": ach, "frac": ach / peak, "traffic": ncu_traffic(name)}
-            line["gpu_launches"] += rs["launches"] + rs["e2e_launches"]
         line["secondary"] = sec
-    line["gpu_launches"] += r["e2e_launches"]
+    try:
+        dense = {}
+        for name in [args.workload] + (SECONDARY if args.workload == DEFAULT and not args.no_secondary else []):
+            ws = WORKLOADS[name]
+            dense[name] = {"ms_per_layer": time_dense_sdpa(ws, device),
+                           "sparse_ms_per_layer": (r["ms_per_step"] if name == args.workload
+                                                   else line["secondary"][name]["ms_per_step"]) / ws["L"]}
+        line["dense_causal_sdpa"] = {"kind": "torch scaled_dot_product_attention, causal, same shape, no RoPE",
+                                     "layers": dense}
+    except Exception as exc:  # the comparison is context only
+        line["dense_causal_sdpa"] = {"unavailable": str(exc)[:200]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         per_layer, desc = time_oracle(w, 3)
         line["cpu_baseline"] = {"value": oracle_tokens_per_s(w, per_layer), "unit": UNIT, "cores": 1,
