@@ -33,7 +33,10 @@
 
 namespace fibattn {
 
-constexpr int kTcWarps = 4;                    // consumer warps
+#ifndef FIB_TC_WARPS
+#define FIB_TC_WARPS 4
+#endif
+constexpr int kTcWarps = FIB_TC_WARPS;         // consumer warps (16 queries each)
 constexpr int kTcTile = 16 * kTcWarps;         // queries per CTA
 constexpr int kConsumers = 32 * kTcWarps;
 constexpr int kTcThreads = kConsumers + 32;    // + one producer warp
@@ -198,7 +201,8 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(TcArgs a) {
+__global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2) : (MODE == 0 ? 5 : 4))
+    fwd_tc_kernel(TcArgs a) {
   __shared__ KeySmem ks;
   __shared__ __align__(8) uint64_t full_bar[kSlots];
   __shared__ __align__(8) uint64_t empty_bar[kSlots];
@@ -312,8 +316,9 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
   // p0 = i0 - 16 instead of their absolute position: the common e^{i p0 theta} cancels in
   // q'_i . k'_j, and the offsets (< 80) need only the small lo table (plus hi row 1).
   // Rows of this thread: Q rows g, g+8 of the warp (offsets 16 + 16 warp + g (+8)) and the
-  // K' conversion tasks (row tid/4 + 32k, frequencies 8t..8t+7 since tid % 4 == t).
-  float2 eq[2][8], ek[3][8];
+  // K' conversion tasks (row tid/4 + (consumers/4) k, frequencies 8t..8t+7 since tid % 4 == t).
+  constexpr int kKTasks = (kWinRows * 4 + kConsumers - 1) / kConsumers;  // K' tasks per thread
+  float2 eq[2][8], ek[kKTasks][8];
   {
     float2 h1[8];  // e^{i 64 theta_m}
     const float4* h4 = reinterpret_cast<const float4*>(a.rope_hi + kFreq + 8 * t);
@@ -343,7 +348,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
 #pragma unroll
     for (int h = 0; h < 2; ++h) rel(16 + 16 * warp + g + 8 * h, eq[h]);
 #pragma unroll
-    for (int k = 0; k < 3; ++k) rel((tid >> 2) + 32 * k, ek[k]);
+    for (int k = 0; k < kKTasks; ++k) rel((tid >> 2) + (kConsumers / 4) * k, ek[k]);
   }
   auto wait_stage = [&](int n) {
     if (!s_err && !mbar_wait(&full_bar[n % kSlots], (n / kSlots) & 1, a.wait_ns)) {
@@ -418,7 +423,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
   uint4* Vs = reinterpret_cast<uint4*>(ring + 2 * a.slot_bytes);
   wait_stage(1);
 #pragma unroll
-  for (int k = 0; k < 3; ++k) {
+  for (int k = 0; k < kKTasks; ++k) {
     const int task = tid + k * kConsumers;
     if (task >= kWinRows * 4) break;
     const int row = task >> 2, c = task & 3;
@@ -445,7 +450,8 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 3 : 2) fwd_tc_kernel(T
   }
   wait_stage(2);
   {
-    constexpr int kVTasks = kWinRows * 8 / kConsumers;  // 5
+    constexpr int kVTasks = kWinRows * 8 / kConsumers;  // 5 (4 warps) or 6 (2 warps)
+    static_assert(kVTasks * kConsumers == kWinRows * 8, "V conversion tasks must divide evenly");
     uint32_t w[kVTasks][4];
 #pragma unroll
     for (int k = 0; k < kVTasks; ++k) {
@@ -708,13 +714,13 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
                           int skip_first_rung_copy, const float* fac_dev, cudaStream_t stream) {
   TcArgs a;
   // the Q rows (8 KB) and the factor tables (256 B per rung, two tables for interp) share a slot
-  const int slot = 2 * (t.mode == 1 ? 72 : 64) * kRowBytes;
+  const int slot = 2 * (t.mode == 1 ? kTcTile + 8 : kTcTile) * kRowBytes;
   const bool fits = kTcTile * kRowBytes + (t.mode == 1 ? 2 : 1) * t.n * 256 <= slot;
   a.fac_dev = fits ? fac_dev : nullptr;
   a.t = t;
   a.N = N;
   a.tiles = (N + kTcTile - 1) / kTcTile;
-  a.slab_rows = t.mode == 1 ? 72 : 64;
+  a.slab_rows = t.mode == 1 ? kTcTile + 8 : kTcTile;
   a.slot_bytes = 2 * a.slab_rows * kRowBytes;
   a.fac_stride = t.n > 0 ? t.n : 1;  // rungs kept <= t.n (device-alpha interp may keep fewer)
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -732,13 +738,18 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const size_t smem = static_cast<size_t>(kSlots) * a.slot_bytes +
                       static_cast<size_t>(t.mode == 1 ? 2 : 1) * a.fac_stride * 64 * sizeof(float);
+  // The opt-in limit is a property of the kernel function, not of a launch: launches that a
+  // CUDA graph captured earlier replay under whatever limit was set last.  So it is always
+  // set to the largest size any launch of this kernel can ask for (all kMaxR rungs).
+  const int smem_max = kSlots * 2 * (t.mode == 1 ? kTcTile + 8 : kTcTile) * kRowBytes +
+                       (t.mode == 1 ? 2 : 1) * kMaxR * 64 * static_cast<int>(sizeof(float));
   cudaError_t e;
   if (t.mode == 0) {
-    e = cudaFuncSetAttribute(fwd_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = cudaFuncSetAttribute(fwd_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     if (e != cudaSuccess) return e;
     fwd_tc_kernel<0><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a);
   } else {
-    e = cudaFuncSetAttribute(fwd_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = cudaFuncSetAttribute(fwd_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     if (e != cudaSuccess) return e;
     fwd_tc_kernel<1><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a);
   }

@@ -351,3 +351,29 @@ def test_starved_stage_times_out_and_context_survives():
     with pytest.raises(fa.FibAttnError):
         fa.fib_attn_plan_set_debug(plan, False, 10)
     plan.close()
+
+
+# ------------------------------------------------------------------ CUDA graph replay
+def test_graph_replay_of_a_stack_with_varying_rung_counts():
+    """Layers of the coprime stack keep 8 to 11 rungs, so their launches need different
+    shared-memory sizes; a captured stack must replay every layer exactly as an eager call."""
+    B, H, N, W = 1, 2, 4096, 12
+    alphas = oracle.schedule("coprime", 16)
+    plan = _plan("fib", alphas, W, N, "mask")
+    xs = [tuple(t.cuda() for t in inputs.qkv(B, H, N, 64, 2, l, "bf16")) for l in range(16)]
+    eager = [fa.fib_attn_fwd(plan, l, *xs[l])[0] for l in range(16)]
+    outs = [torch.empty_like(x[0]) for x in xs]
+    lses = [torch.empty(B, H, N, device="cuda") for _ in xs]
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for l in range(16):
+            fa.fib_attn_fwd(plan, l, *xs[l], o=outs[l], lse=lses[l])
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for l in range(16):
+        assert torch.equal(outs[l], eager[l]), l
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    plan.close()
