@@ -50,6 +50,7 @@ struct TcArgs {
   LayerTable t;
   int N;
   int tiles;
+  int bh;  // B * H
   int slab_rows;   // rows of a rung slab region: 64 (mask) or 72 (interp: 65 used)
   int slot_bytes;  // 2 * slab_rows * 128
   int fac_stride;  // rungs per factor table (second table for interp rows lo+1)
@@ -212,8 +213,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
   unsigned char* ring = smem;
   float* fac = reinterpret_cast<float*>(smem + kSlots * a.slot_bytes);  // cos[32], sin[32] per rung
 
-  const int bh = blockIdx.x / a.tiles;
-  const int tile = blockIdx.x - bh * a.tiles;
+  // Heaviest tiles first: a later tile attends more rungs (d <= i), so launching the tiles
+  // from the end of the sequence backwards leaves the light ones for the last partial wave.
+  const int bh = blockIdx.x % a.bh;
+  const int tile = a.tiles - 1 - static_cast<int>(blockIdx.x / a.bh);
   const int i0 = tile * kTcTile;
   const int N = a.N;
   const int tid = threadIdx.x;
@@ -720,6 +723,7 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   a.t = t;
   a.N = N;
   a.tiles = (N + kTcTile - 1) / kTcTile;
+  a.bh = B * H;
   a.slab_rows = t.mode == 1 ? kTcTile + 8 : kTcTile;
   a.slot_bytes = 2 * a.slab_rows * kRowBytes;
   a.fac_stride = t.n > 0 ? t.n : 1;  // rungs kept <= t.n (device-alpha interp may keep fewer)
