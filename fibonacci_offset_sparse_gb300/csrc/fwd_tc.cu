@@ -240,7 +240,11 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
   const int nr = ks.nr;
 
   const int warp = tid >> 5, lane = tid & 31;
-  const int n_stages = 3 + nr;  // Q, window K, window V, then one per rung
+  // Rungs are kept in ascending distance; the tile streams rungs [0, nrt), up to the last one
+  // that some row of it attends (a later tile attends more).
+  const unsigned attended = __ballot_sync(0xffffffffu, lane < nr && ks.need[W + lane] <= i_last);
+  const int nrt = 32 - __clz(static_cast<int>(attended));
+  const int n_stages = 3 + nrt;  // Q, window K, window V, then one per streamed rung
 
   // ===================================================================== producer
   if (warp == kTcWarps) {
@@ -570,19 +574,19 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
   int srow[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) srow[h] = ic[h] - i0 + (MODE == 1 ? 1 : 0);
-  for (int r0 = 0; r0 < nr; r0 += kRungChunk) {
+  for (int r0 = 0; r0 < nrt; r0 += kRungChunk) {
 #pragma unroll
     for (int cc = 0; cc < kRungChunk; ++cc)
-      if (r0 + cc < nr) wait_stage(3 + r0 + cc);
+      if (r0 + cc < nrt) wait_stage(3 + r0 + cc);
     float sc[2][kRungChunk];
     bool act[kRungChunk];
     int rowu[2][kRungChunk], fcop[kRungChunk];
 #pragma unroll
     for (int cc = 0; cc < kRungChunk; ++cc) {
-      const int r = r0 + cc < nr ? r0 + cc : r0;
+      const int r = r0 + cc < nrt ? r0 + cc : r0;
       const int c = W + r;
       const int lo = ks.lo[c];
-      const bool in = (r0 + cc < nr) && !s_err;
+      const bool in = (r0 + cc < nrt) && !s_err;
       bool ok[2];
       // first copied row of this slab (slab rows start at global row i0 - lo - interp)
       const int first_copied = max(0, lo - i0 + (MODE == 1 ? 1 : 0));
@@ -681,7 +685,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
     }
 #pragma unroll
     for (int cc = 0; cc < kRungChunk; ++cc)
-      if (r0 + cc < nr) release_stage(3 + r0 + cc);
+      if (r0 + cc < nrt) release_stage(3 + r0 + cc);
   }
 
   // ---- epilogue (nothing is written after a wait gave up; the producer reports it)

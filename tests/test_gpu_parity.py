@@ -330,7 +330,7 @@ def test_edge_cases_bf16(mode, N, W, alpha, kind):
 
 # ------------------------------------------------------------------ bounded waits
 def test_starved_stage_times_out_and_context_survives():
-    """The hook leaves the first rung stage of every CTA without its copy; each CTA's wait
+    """The hook leaves the first rung stage of every CTA (each attends d = 13) without its copy; each CTA's wait
     gives up after 2 ms, records FIB_ERR_TIMEOUT and exits.  The same context then runs a
     normal forward that matches the oracle."""
     B, H, N, W, alpha = 1, 2, 256, 12, 1.0
