@@ -20,10 +20,11 @@ cudaError_t launch_fwd(const LayerTable& t, int B, int H, int N, int dtype, cons
                        const void* k, const void* v, void* o, float* lse, const float2* lo_tab,
                        const float2* hi_tab, cudaStream_t stream);
 bool tc_supported(const LayerTable& t);
+size_t fwd_tc_workspace_bytes(int B, int H, int N);
 cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k,
                           const void* v, void* o, float* lse, const float2* lo_tab,
                           const float2* hi_tab, int* status, unsigned long long wait_ns,
-                          int skip_first_rung_copy, const float* fac_dev, cudaStream_t stream);
+                          int skip_first_rung_copy, void* workspace, cudaStream_t stream);
 cudaError_t launch_debug_indices(const LayerTable& t, int N, int i0, int i1, int32_t* out,
                                  float* w_out, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int H, int N);
@@ -52,10 +53,6 @@ struct fib_attn_plan_s {
   int* d_status = nullptr;
   unsigned long long wait_ns = 1000000000ULL;  // bound of every device-side wait (1 s)
   int skip_first_rung_copy = 0;                // test hook, see fib_attn_plan_set_debug
-  // per layer, the rungs at N_max and their RoPE factors cos/sin(lo theta_m) and
-  // cos/sin((lo+1) theta_m), binary64-built, on the device: [layer][2][kMaxR][64] floats
-  std::vector<std::vector<int32_t>> rungs_at_nmax;
-  float* d_fac = nullptr;
 };
 
 namespace {
@@ -100,18 +97,6 @@ int make_table(const fib_attn_plan_s* p, int layer, int N, const float* alpha_de
     t->alpha_dev = alpha_dev;
   }
   return FIB_OK;
-}
-
-// Device factor table of `layer` if the call's rungs are the plan's rungs at N_max or a
-// prefix of them (the usual case: a shorter N only drops the longest distances); else null,
-// and the kernel derives the factors itself.
-const float* layer_factors(const fib_attn_plan_s* p, int layer, const LayerTable& t) {
-  if (p->d_fac == nullptr || t.alpha_dev != nullptr) return nullptr;
-  const std::vector<int32_t>& ref = p->rungs_at_nmax[layer];
-  if (t.n > static_cast<int>(ref.size())) return nullptr;
-  for (int r = 0; r < t.n; ++r)
-    if (t.lo[r] != ref[r]) return nullptr;
-  return p->d_fac + static_cast<size_t>(layer) * 2 * kMaxR * 64;
 }
 
 int check_device(const fib_attn_plan_s* p) {
@@ -262,28 +247,9 @@ int fib_attn_plan_create(fib_attn_plan_t* out, int base_kind, const int32_t* cus
   }
   std::vector<float> lo, hi;
   rope_tables(N_max, rope_base, &lo, &hi);
-  std::vector<float> fac(static_cast<size_t>(n_layers) * 2 * kMaxR * 64, 0.f);
-  p->rungs_at_nmax.resize(n_layers);
-  for (int l = 0; l < n_layers; ++l) {
-    LayerTable t;
-    make_table(p, l, N_max, nullptr, &t);
-    p->rungs_at_nmax[l].assign(t.lo, t.lo + t.n);
-    for (int r = 0; r < t.n; ++r)
-      for (int m = 0; m < kFreq; ++m) {
-        const double theta = std::pow(rope_base, -2.0 * m / kD);
-        for (int tab = 0; tab < 2; ++tab) {
-          const double ang = static_cast<double>(t.lo[r] + tab) * theta;
-          float* row = &fac[((static_cast<size_t>(l) * 2 + tab) * kMaxR + r) * 64];
-          row[m] = static_cast<float>(std::cos(ang));
-          row[32 + m] = static_cast<float>(std::sin(ang));
-        }
-      }
-  }
   cudaError_t e = cudaMalloc(&p->d_lo, lo.size() * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&p->d_hi, hi.size() * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&p->d_status, sizeof(int));
-  if (e == cudaSuccess) e = cudaMalloc(&p->d_fac, fac.size() * sizeof(float));
-  if (e == cudaSuccess) e = cudaMemcpy(p->d_fac, fac.data(), fac.size() * sizeof(float), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(p->d_lo, lo.data(), lo.size() * sizeof(float), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(p->d_hi, hi.data(), hi.size() * sizeof(float), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(int));
@@ -291,7 +257,6 @@ int fib_attn_plan_create(fib_attn_plan_t* out, int base_kind, const int32_t* cus
     cudaFree(p->d_lo);
     cudaFree(p->d_hi);
     cudaFree(p->d_status);
-    cudaFree(p->d_fac);
     delete p;
     return cuda_status(e);
   }
@@ -308,7 +273,6 @@ int fib_attn_plan_destroy(fib_attn_plan_t p) {
   cudaFree(p->d_lo);
   cudaFree(p->d_hi);
   cudaFree(p->d_status);
-  cudaFree(p->d_fac);
   if (prev >= 0) cudaSetDevice(prev);
   delete p;
   return FIB_OK;
@@ -326,11 +290,21 @@ int fib_attn_plan_distances(fib_attn_plan_t p, int layer, int N, int32_t* out, i
   return FIB_OK;
 }
 
+size_t fib_attn_fwd_workspace_size(fib_attn_plan_t p, int B, int H, int N, int dtype) {
+  if (p == nullptr || B < 1 || H < 1 || N < 1 || dtype != FIB_DTYPE_BF16 || p->W > 16) return 0;
+  return fwd_tc_workspace_bytes(B, H, N);
+}
+
 int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, const void* q,
                  const void* k, const void* v, void* o, float* lse, const float* alpha_dev,
-                 void* stream) {
+                 void* workspace, size_t ws_bytes, void* stream) {
   int st = check_shape(p, layer, B, H, N, dtype);
   if (st != FIB_OK) return st;
+  const size_t need = fib_attn_fwd_workspace_size(p, B, H, N, dtype);
+  if (need > 0 && (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < need))
+    return FIB_ERR_INVALID_ARG;
+  if (need > 0 && (workspace == q || workspace == k || workspace == v || workspace == o))
+    return FIB_ERR_INVALID_ARG;
   if (check_tensor(q) || check_tensor(k) || check_tensor(v) || check_tensor(o)) return FIB_ERR_INVALID_ARG;
   if (o == q || o == k || o == v) return FIB_ERR_INVALID_ARG;
   if (lse != nullptr && !aligned(lse, 4)) return FIB_ERR_INVALID_ARG;
@@ -340,12 +314,11 @@ int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, c
   LayerTable t;
   st = make_table(p, layer, N, p->mode == FIB_MODE_INTERP ? alpha_dev : nullptr, &t);
   if (st != FIB_OK) return st;
-  // bf16 with a window of at most 16 keys: window band on tensor cores (fwd_tc.cu);
-  // otherwise the CUDA-core kernel (fwd.cu), which also serves float32 exactly.
+  // bf16 with a window of at most 16 keys: K'/V' preparation plus the tensor-core kernel
+  // (fwd_tc.cu); otherwise the CUDA-core kernel (fwd.cu), which also serves float32 exactly.
   if (dtype == FIB_DTYPE_BF16 && tc_supported(t))
     return cuda_status(launch_fwd_tc(t, B, H, N, q, k, v, o, lse, p->d_lo, p->d_hi, p->d_status,
-                                     p->wait_ns, p->skip_first_rung_copy,
-                                     layer_factors(p, layer, t),
+                                     p->wait_ns, p->skip_first_rung_copy, workspace,
                                      static_cast<cudaStream_t>(stream)));
   return cuda_status(launch_fwd(t, B, H, N, dtype, q, k, v, o, lse, p->d_lo, p->d_hi,
                                 static_cast<cudaStream_t>(stream)));

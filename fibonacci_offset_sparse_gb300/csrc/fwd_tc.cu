@@ -1,62 +1,65 @@
-// bf16 forward kernel (sm_103a): window band on tensor cores, rungs on CUDA cores, every
-// K/V row staged into shared memory by the bulk-copy engine.
+// bf16 forward (sm_103a): RoPE'd keys and f16 values prepared once per layer, then the
+// window band and every rung on tensor cores, every row staged in shared memory by the
+// bulk-copy engine.
 //
 // Same operation as fwd.cu ("Depth-Staggered Fibonacci Spacing for Sparse Attention",
-// Methodology > "Attended set", "Scaling", "Implementation"), split by where the work is
-// dense:
-//   * window band: for a warp's 16 consecutive queries every window key lies in the
-//     32-row block [q0-16, q0+16) (W <= 16), so S = Q' K'^T and O = P V run as
-//     mma.sync m16n8k16 (f16 operands, f32 accumulation).  Q' and K' are RoPE-rotated at
-//     their own positions once per staged row; V is staged as f16.
-//   * rungs: a rung is a shifted diagonal (query i reads row i-d); it has no dense block,
-//     so those pairs run on the CUDA cores with packed f32x2 arithmetic, applying RoPE in
-//     relative form: q'_i . k'_{i-d} = sum_m z_m . k_m with z_m the raw query pair rotated
-//     by d theta_m and k_m the raw key pair (rotate-half pairs (m, m+32)).
-//   * data movement: a CTA owns 64 consecutive queries of one (b,h) and is warp-specialised:
-//     4 consumer warps compute, 1 producer thread streams every row they read through a
-//     4-slot shared-memory ring with cp.async.bulk (mbarrier completion): the Q rows, the
-//     raw window K and V rows [i0-16, i0+64), then per rung the slab rows [i0-d, i0-d+64)
-//     of K and V (two contiguous runs).  The producer runs up to 4 slots ahead and refills a
-//     slot as soon as the 4 consumer warps release it; the window rows are converted in
-//     place inside their slots, so the ring is nearly all of the CTA's shared memory and 3
-//     CTAs fit on an SM.  Every mbarrier wait is bounded in time; a wait that gives up
-//     records FIB_ERR_TIMEOUT in the plan's status word, the consumers stop, and the producer
+// Methodology > "Attended set", "Scaling", "Implementation"), in two launches:
+//   * prep_kv_kernel streams K and V once: K' = RoPE(K) at each row's own position and
+//     V' = V, both rounded to f16, rows stored chunk-swizzled (below).  A key row is read
+//     by its window band and by one query per rung, so rotating and converting it once
+//     here replaces a rotation and a conversion per (query, rung) in the attention kernel.
+//   * fwd_tc_kernel: a CTA owns 64 consecutive queries of one (b,h): 4 compute warps of 16
+//     queries plus one producer thread that streams the rows they read through a 3-slot
+//     shared-memory ring with cp.async.bulk (mbarrier completion): the Q rows, the window
+//     rows [i0-16, i0+64) of K' and V', then per rung the slab rows [i0-d, i0-d+64) of K'
+//     and V'.  The producer runs up to 3 slots ahead and refills a slot once the 4 compute
+//     warps release it (3 slots of 16 KB and 96 registers a thread let 4 CTAs share an SM).  Every mbarrier wait is bounded in time; a wait that gives up
+//     records FIB_ERR_TIMEOUT in the plan's status word, the warps stop, and the producer
 //     lets its copies in flight land before the CTA exits.
-// Register layout: lane (g = lane/4, t = lane%4) owns query rows g and g+8 of its warp's 16
-// and the dims D_t = [8t, 8t+8) u [32+8t, 32+8t+8) (RoPE partners in the same lane).  The
-// MMA k-order is permuted so that a lane's A/B fragments hold exactly D_t, and V's columns
-// are permuted so that its O accumulator fragment is D_t too: the CUDA-core rung updates
-// and the tensor-core window update share the O registers.
+//   * window band: for a warp's 16 queries every window key lies in the 32-row block
+//     [q0-16, q0+16) (W <= 16): S = Q' K'^T and O = P V' as mma.sync m16n8k16 (f16
+//     operands, f32 accumulation), Q' rotated at its own position and scaled by
+//     log2(e)/sqrt(D) so that scores are in log2 units.
+//   * rungs: query i reads slab row i - i0 (+1 for interp), so a rung is the diagonal of a
+//     16x16 block: S_r = diag(Q' K'_slab^T) takes 8 MMAs (2 key n-tiles x 4 k-steps) whose
+//     diagonal is picked out, and O += diag(P) V'_slab takes 8 more (A = diag(P) in f16).
+//     The tensor pipe does 16x the needed products, but it replaces ~250 CUDA-core
+//     instructions per warp and rung (RoPE of the query, bf16 unpacking, dot products,
+//     axpys) with ~40.
+// Register layout: lane (g = lane/4, t = lane%4) owns query rows g and g+8 of its warp.  For
+// the score MMAs the k-order is permuted so that a lane's A fragments hold the dims
+// D_t = [8t, 8t+8) u [32+8t, 32+8t+8) (RoPE partners in the same lane) and its B fragments
+// the same dims of one key row (two 16-byte chunks).  O is in the natural accumulator
+// layout: n-tile nt of row g holds dims 8nt+2t, 8nt+2t+1.
+// Shared/global row layout of K' and V': the 16-byte chunk c (dims 8c..8c+7) of the row of
+// sequence position p sits at chunk c ^ swz(p), swz(p) = 4(p&1) | ((p>>1)&3).  Eight
+// consecutive rows put a given chunk in 8 distinct bank groups (ldmatrix of V'), and two
+// consecutive rows put chunks {0..3} in opposite halves (the 16-byte loads of K').
 #include <cuda_fp16.h>
 
 #include "common.cuh"
 
 namespace fibattn {
 
-#ifndef FIB_TC_WARPS
-#define FIB_TC_WARPS 4
-#endif
-constexpr int kTcWarps = FIB_TC_WARPS;         // consumer warps (16 queries each)
+constexpr int kTcWarps = 4;                    // compute warps (16 queries each)
 constexpr int kTcTile = 16 * kTcWarps;         // queries per CTA
 constexpr int kConsumers = 32 * kTcWarps;
 constexpr int kTcThreads = kConsumers + 32;    // + one producer warp
-constexpr int kWinRows = kTcTile + 16;         // window rows [i0-16, i0+64)
 constexpr int kTcMaxW = 16;
-constexpr int kSlots = 4;                      // ring slots
+constexpr int kSlots = 3;                      // ring slots
 constexpr int kRungChunk = 2;                  // rungs per online-softmax step
-constexpr int kRowBytes = kD * 2;              // one bf16 row
+constexpr int kRowBytes = kD * 2;              // one row of 16-bit values
 
 struct TcArgs {
   LayerTable t;
   int N;
   int tiles;
-  int bh;  // B * H
+  int bh;          // B * H
   int slab_rows;   // rows of a rung slab region: 64 (mask) or 72 (interp: 65 used)
   int slot_bytes;  // 2 * slab_rows * 128
-  int fac_stride;  // rungs per factor table (second table for interp rows lo+1)
   const __nv_bfloat16* q;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
+  const __half* kp;  // K' rows (prep_kv_kernel)
+  const __half* vp;  // V' rows
   __nv_bfloat16* o;
   float* lse;
   const float2* rope_lo;
@@ -65,10 +68,6 @@ struct TcArgs {
   int* status;                 // plan status word (FIB_ERR_TIMEOUT on a wait that gave up)
   unsigned long long wait_ns;  // bound of every mbarrier wait
   int skip_first_rung_copy;    // test hook: never arrive on rung 0's stage
-  // Rung factors cos / sin of (lo theta_m) and, for interp, of ((lo+1) theta_m), built in
-  // binary64 by the plan: table 0 at fac_dev[r*64 + {0..31: cos, 32..63: sin}], table 1 at
-  // fac_dev[(kMaxR + r)*64 + ...].  Null: computed here from the RoPE tables.
-  const float* fac_dev;
 };
 
 // ------------------------------------------------------------------ small PTX helpers
@@ -106,7 +105,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   }
 }
 // The producer's wait: like mbar_wait, but it backs off with __nanosleep between polls so
-// that a waiting producer leaves the issue slots to the consumer warps of its SM.
+// that a waiting producer leaves the issue slots to the compute warps of its SM.
 __device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
   if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
@@ -125,16 +124,25 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;\n" ::"n"(kConsumers) : "memory");
+}
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
-__device__ __forceinline__ float2 bf2(uint32_t w) { return make_float2(bf_lo(w), bf_hi(w)); }
+__device__ __forceinline__ uint32_t pack_bf2_rn(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -146,6 +154,9 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* smem
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(smem_addr(smem_row)));
 }
+
+// Chunk swizzle of the K'/V' row of sequence position p (p >= 0 where it matters).
+__device__ __forceinline__ int swz(int p) { return ((p & 1) << 2) | ((p >> 1) & 3); }
 
 // Read the 16 dims D_t of a 128-byte bf16 row in shared memory as two 16-byte words;
 // odd rows read their halves in the opposite order, so the 8 lanes of a phase (two rows
@@ -162,48 +173,76 @@ __device__ __forceinline__ void lds_row_part(const unsigned char* row, int t, bo
   }
 }
 
-// Score partial of one row: sum over the lane's 4 frequency pairs of z1 k1 + z2 k2 with
-// z = q e^{i d theta} (cs = cos, sn = sin of d theta for the lane's frequencies).
-__device__ __forceinline__ float rung_dot(const float2 (&q1)[4], const float2 (&q2)[4],
-                                          const float2 (&cs)[4], const float2 (&sn)[4],
-                                          const float2 (&ns)[4], const uint4& ka, const uint4& kb) {
+// The dims D_t of the swizzled K' row of position p, as the B fragments of the 4 k-steps.
+__device__ __forceinline__ void lds_kfrag(const uint4* row, int t, int p, uint32_t (&lo)[4],
+                                          uint32_t (&hi)[4]) {
+  const int s = swz(p);
+  const uint4 a = row[t ^ s], b = row[(t + 4) ^ s];
+  lo[0] = a.x; lo[1] = a.y; lo[2] = a.z; lo[3] = a.w;
+  hi[0] = b.x; hi[1] = b.y; hi[2] = b.z; hi[3] = b.w;
+}
+
+// e^{i p theta_m} for the lane's frequencies m = 8t .. 8t+7, from the factored tables.
+__device__ __forceinline__ void rope_row(const float2* __restrict__ lo_tab, const float2* __restrict__ hi_tab,
+                                         int p, int t, float2 (&e)[8]) {
+  const float4* h4 = reinterpret_cast<const float4*>(hi_tab + (p / kSplit) * kFreq + 8 * t);
+  const float4* l4 = reinterpret_cast<const float4*>(lo_tab + (p % kSplit) * kFreq + 8 * t);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float4 x = __ldg(h4 + u), y = __ldg(l4 + u);
+    e[2 * u] = make_float2(x.x * y.x - x.y * y.y, x.x * y.y + x.y * y.x);
+    e[2 * u + 1] = make_float2(x.z * y.z - x.w * y.w, x.z * y.w + x.w * y.z);
+  }
+}
+
+// ------------------------------------------------------------------ K', V' preparation
+// One thread per (row, quarter u): frequencies m = 8u .. 8u+7, i.e. chunks u (dims 8u..) and
+// u+4 (their rotate-half partners 32+8u..) of the K row, and the same two chunks of V.
+__global__ void __launch_bounds__(256) prep_kv_kernel(const __nv_bfloat16* __restrict__ k,
+                                                      const __nv_bfloat16* __restrict__ v,
+                                                      __half* __restrict__ kp, __half* __restrict__ vp,
+                                                      const float2* __restrict__ lo_tab,
+                                                      const float2* __restrict__ hi_tab, int N,
+                                                      long long rows) {
+  const long long gid = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  const long long row = gid >> 2;
+  if (row >= rows) return;
+  const int u = static_cast<int>(gid & 3);
+  const int p = static_cast<int>(row % N);
+  const uint4* k4 = reinterpret_cast<const uint4*>(k + row * kD);
+  const uint4* v4 = reinterpret_cast<const uint4*>(v + row * kD);
+  const uint4 ka = __ldg(k4 + u), kb = __ldg(k4 + u + 4), va = __ldg(v4 + u), vb = __ldg(v4 + u + 4);
+  float2 e[8];
+  rope_row(lo_tab, hi_tab, p, u, e);
   const uint32_t xa[4] = {ka.x, ka.y, ka.z, ka.w}, xb[4] = {kb.x, kb.y, kb.z, kb.w};
-  float2 acc1 = make_float2(0.f, 0.f), acc2 = make_float2(0.f, 0.f);
+  uint32_t ya[4], yb[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float2 k1 = bf2(xa[j]), k2 = bf2(xb[j]);
-    // z = q e^{i d theta}: z1 = c q1 - s q2, z2 = s q1 + c q2
-    const float2 z1 = __ffma2_rn(ns[j], q2[j], __fmul2_rn(cs[j], q1[j]));
-    const float2 z2 = __ffma2_rn(cs[j], q2[j], __fmul2_rn(sn[j], q1[j]));
-    acc1 = __ffma2_rn(z1, k1, acc1);
-    acc2 = __ffma2_rn(z2, k2, acc2);
+    // (k_m, k_{m+32}) -> (k_m c - k_{m+32} s, k_m s + k_{m+32} c), m = 8u + 2j (+1)
+    const float k1x = bf_lo(xa[j]), k1y = bf_hi(xa[j]), k2x = bf_lo(xb[j]), k2y = bf_hi(xb[j]);
+    const float2 e0 = e[2 * j], e1 = e[2 * j + 1];
+    ya[j] = pack_h2(k1x * e0.x - k2x * e0.y, k1y * e1.x - k2y * e1.y);
+    yb[j] = pack_h2(k1x * e0.y + k2x * e0.x, k1y * e1.y + k2y * e1.x);
   }
-  return (acc1.x + acc2.x) + (acc1.y + acc2.y);
+  const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+  uint32_t za[4], zb[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    za[j] = pack_h2(bf_lo(wa[j]), bf_hi(wa[j]));
+    zb[j] = pack_h2(bf_lo(wb[j]), bf_hi(wb[j]));
+  }
+  const int s = swz(p);
+  uint4* ko = reinterpret_cast<uint4*>(kp + row * kD);
+  uint4* vo = reinterpret_cast<uint4*>(vp + row * kD);
+  ko[u ^ s] = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+  ko[(u + 4) ^ s] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+  vo[u ^ s] = make_uint4(za[0], za[1], za[2], za[3]);
+  vo[(u + 4) ^ s] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
 }
 
-__device__ __forceinline__ void load_fac(const float* f, int t, float2 (&cs)[4], float2 (&sn)[4]) {
-  const float4* f4 = reinterpret_cast<const float4*>(f);
-  const float4 ca = f4[2 * t], cb = f4[2 * t + 1], sa = f4[8 + 2 * t], sb = f4[8 + 2 * t + 1];
-  cs[0] = make_float2(ca.x, ca.y);
-  cs[1] = make_float2(ca.z, ca.w);
-  cs[2] = make_float2(cb.x, cb.y);
-  cs[3] = make_float2(cb.z, cb.w);
-  sn[0] = make_float2(sa.x, sa.y);
-  sn[1] = make_float2(sa.z, sa.w);
-  sn[2] = make_float2(sb.x, sb.y);
-  sn[3] = make_float2(sb.z, sb.w);
-}
-
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;\n" ::"n"(kConsumers) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
-}
-
+// ------------------------------------------------------------------ attention kernel
 template <int MODE>
-__global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2) : (MODE == 0 ? 5 : 4))
-    fwd_tc_kernel(TcArgs a) {
+__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 4 : 3) fwd_tc_kernel(TcArgs a) {
   __shared__ KeySmem ks;
   __shared__ __align__(8) uint64_t full_bar[kSlots];
   __shared__ __align__(8) uint64_t empty_bar[kSlots];
@@ -211,7 +250,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
   extern __shared__ __align__(128) unsigned char smem[];
   const int SR = a.slab_rows;
   unsigned char* ring = smem;
-  float* fac = reinterpret_cast<float*>(smem + kSlots * a.slot_bytes);  // cos[32], sin[32] per rung
+  constexpr int kI = MODE == 1 ? 1 : 0;  // interp: the slab starts one row earlier
 
   // Heaviest tiles first: a later tile attends more rungs (d <= i), so launching the tiles
   // from the end of the sequence backwards leaves the light ones for the last partial wave.
@@ -222,9 +261,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
   const int tid = threadIdx.x;
   const size_t base = static_cast<size_t>(bh) * N * kD;
   const __nv_bfloat16* __restrict__ Q = a.q + base;
-  const __nv_bfloat16* __restrict__ K = a.k + base;
-  const __nv_bfloat16* __restrict__ V = a.v + base;
+  const __half* __restrict__ Kp = a.kp + base;
+  const __half* __restrict__ Vp = a.vp + base;
   const int i_last = min(i0 + kTcTile, N) - 1;  // last real query of the tile
+  const int w0 = max(i0 - 16, 0);                // first copied window row
 
   build_keys(a.t, N, &ks);
   if (tid == 0) {
@@ -244,7 +284,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
   // that some row of it attends (a later tile attends more).
   const unsigned attended = __ballot_sync(0xffffffffu, lane < nr && ks.need[W + lane] <= i_last);
   const int nrt = 32 - __clz(static_cast<int>(attended));
-  const int n_stages = 3 + nrt;  // Q, window K, window V, then one per streamed rung
+  const int n_stages = 3 + nrt;  // Q, window K', window V', then one per streamed rung
 
   // ===================================================================== producer
   if (warp == kTcWarps) {
@@ -252,7 +292,6 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
     int last_n[kSlots];
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) last_n[s] = -1;
-    const int w0 = max(i0 - 16, 0);
     for (int n = 0; n < n_stages; ++n) {
       if (s_err) break;
       const int slot = n % kSlots;
@@ -261,33 +300,27 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
         break;
       }
       unsigned char* dst = ring + slot * a.slot_bytes;
-      if (n == 0) {  // Q rows [i0, i_last]; then the plan's rung factor tables, if any
+      if (n == 0) {  // Q rows [i0, i_last]
         const uint32_t bytes = static_cast<uint32_t>(i_last - i0 + 1) * kRowBytes;
-        const uint32_t fbytes = a.fac_dev != nullptr ? static_cast<uint32_t>(nr) * 256u : 0u;
-        mbar_arrive_tx(&full_bar[slot], bytes + (MODE == 1 ? 2 : 1) * fbytes);
+        mbar_arrive_tx(&full_bar[slot], bytes);
         bulk_g2s(dst, Q + static_cast<size_t>(i0) * kD, bytes, &full_bar[slot]);
-        if (fbytes) {
-          bulk_g2s(dst + kTcTile * kRowBytes, a.fac_dev, fbytes, &full_bar[slot]);
-          if (MODE == 1)  // table 1 packed right after table 0
-            bulk_g2s(dst + kTcTile * kRowBytes + fbytes, a.fac_dev + kMaxR * 64, fbytes, &full_bar[slot]);
-        }
-      } else if (n <= 2) {  // raw window rows [max(i0-16, 0), i_last] of K (n = 1) or V (n = 2)
+      } else if (n <= 2) {  // window rows [w0, i_last] of K' (n = 1) or V' (n = 2)
         const uint32_t bytes = static_cast<uint32_t>(i_last + 1 - w0) * kRowBytes;
         mbar_arrive_tx(&full_bar[slot], bytes);
-        bulk_g2s(dst + (w0 - (i0 - 16)) * kRowBytes, (n == 1 ? K : V) + static_cast<size_t>(w0) * kD, bytes,
-                 &full_bar[slot]);
-      } else {  // rung slab: rows [first, first + SR) of K, then of V, where inside [0, N)
+        bulk_g2s(dst + (w0 - (i0 - 16)) * kRowBytes, (n == 1 ? Kp : Vp) + static_cast<size_t>(w0) * kD,
+                 bytes, &full_bar[slot]);
+      } else {  // rung slab: rows [first, first + SR) of K', then of V', where inside [0, N)
         const int r = n - 3;
         if (r == 0 && a.skip_first_rung_copy) continue;  // test hook: this stage never completes
         const int lo = ks.lo[W + r];
-        const int first = i0 - lo - (MODE == 1 ? 1 : 0);
+        const int first = i0 - lo - kI;
         const int r0 = max(first, 0);
         const int r1 = i_last - lo + 1;
         const uint32_t bytes = r1 > r0 ? static_cast<uint32_t>(r1 - r0) * kRowBytes : 0u;
         mbar_arrive_tx(&full_bar[slot], 2 * bytes);
         if (bytes) {
-          bulk_g2s(dst + (r0 - first) * kRowBytes, K + static_cast<size_t>(r0) * kD, bytes, &full_bar[slot]);
-          bulk_g2s(dst + (SR + r0 - first) * kRowBytes, V + static_cast<size_t>(r0) * kD, bytes,
+          bulk_g2s(dst + (r0 - first) * kRowBytes, Kp + static_cast<size_t>(r0) * kD, bytes, &full_bar[slot]);
+          bulk_g2s(dst + (SR + r0 - first) * kRowBytes, Vp + static_cast<size_t>(r0) * kD, bytes,
                    &full_bar[slot]);
         }
       }
@@ -301,61 +334,16 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
     return;
   }
 
-  // ===================================================================== consumers
+  // ===================================================================== compute warps
   const int g = lane >> 2, t = lane & 3;
   const int q0 = i0 + 16 * warp;
-  // Every factor load is issued here, before the first stage wait, so that its latency
-  // overlaps the first copies.  (1) rung factors e^{i lo theta} into shared memory, from the
-  // kernel parameters when the host built them, else from the RoPE tables;
-  for (int idx = a.fac_dev != nullptr ? nr * kFreq : tid; idx < nr * kFreq; idx += kConsumers) {
-    const int r = idx / kFreq, m = idx % kFreq;
-    const int lo = ks.lo[W + r];
-    const float2 e = rope_factor(a.rope_lo, a.rope_hi, lo, m);
-    fac[r * 64 + m] = e.x;
-    fac[r * 64 + 32 + m] = e.y;
-    if (MODE == 1) {
-      const float2 e1 = rope_factor(a.rope_lo, a.rope_hi, lo + 1, m);
-      fac[(a.fac_stride + r) * 64 + m] = e1.x;
-      fac[(a.fac_stride + r) * 64 + 32 + m] = e1.y;
-    }
-  }
-  // (2) window rotation factors.  Q' and K' are rotated by their offset from the tile base
-  // p0 = i0 - 16 instead of their absolute position: the common e^{i p0 theta} cancels in
-  // q'_i . k'_j, and the offsets (< 80) need only the small lo table (plus hi row 1).
-  // Rows of this thread: Q rows g, g+8 of the warp (offsets 16 + 16 warp + g (+8)) and the
-  // K' conversion tasks (row tid/4 + (consumers/4) k, frequencies 8t..8t+7 since tid % 4 == t).
-  constexpr int kKTasks = (kWinRows * 4 + kConsumers - 1) / kConsumers;  // K' tasks per thread
-  float2 eq[2][8], ek[kKTasks][8];
-  {
-    float2 h1[8];  // e^{i 64 theta_m}
-    const float4* h4 = reinterpret_cast<const float4*>(a.rope_hi + kFreq + 8 * t);
+  int irow[2], ic[2];
+  float2 eq[2][8];  // e^{i p theta_m} of the lane's two query rows (loads overlap the copies)
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float4 x = __ldg(h4 + u);
-      h1[2 * u] = make_float2(x.x, x.y);
-      h1[2 * u + 1] = make_float2(x.z, x.w);
-    }
-    auto rel = [&](int off, float2 (&e)[8]) {
-      const int o = off < kWinRows ? off : 0;
-      const float4* l4 = reinterpret_cast<const float4*>(a.rope_lo + (o & 63) * kFreq + 8 * t);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float4 x = __ldg(l4 + u);
-        e[2 * u] = make_float2(x.x, x.y);
-        e[2 * u + 1] = make_float2(x.z, x.w);
-      }
-      if (o >= 64) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float2 b = e[u];
-          e[u] = make_float2(h1[u].x * b.x - h1[u].y * b.y, h1[u].x * b.y + h1[u].y * b.x);
-        }
-      }
-    };
-#pragma unroll
-    for (int h = 0; h < 2; ++h) rel(16 + 16 * warp + g + 8 * h, eq[h]);
-#pragma unroll
-    for (int k = 0; k < kKTasks; ++k) rel((tid >> 2) + (kConsumers / 4) * k, ek[k]);
+  for (int h = 0; h < 2; ++h) {
+    irow[h] = q0 + g + 8 * h;
+    ic[h] = irow[h] < N ? irow[h] : N - 1;
+    rope_row(a.rope_lo, a.rope_hi, ic[h], t, eq[h]);
   }
   auto wait_stage = [&](int n) {
     if (!s_err && !mbar_wait(&full_bar[n % kSlots], (n / kSlots) & 1, a.wait_ns)) {
@@ -368,137 +356,56 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
     if (lane == 0) mbar_arrive(&empty_bar[n % kSlots]);
   };
 
-  // ---- stage 0: Q rows -> raw q (for the rungs) and rotated f16 A fragments (window)
-  int irow[2], ic[2];
-  float2 q1[2][4], q2[2][4];  // raw q * qscale: (dims 8t+2j, 8t+2j+1) and their partners
-  uint32_t qa[2][2][4];       // A fragments: [row h][dim half][k-step]
+  // ---- stage 0: Q rows -> Q' = RoPE(q) * log2(e)/sqrt(D) as f16 A fragments
+  uint32_t qa[2][2][4];  // [row h][dim half][k-step]
   wait_stage(0);
-  {
-    const unsigned char* qst = ring;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      irow[h] = q0 + g + 8 * h;
-      ic[h] = irow[h] < N ? irow[h] : N - 1;
-      const int row = ic[h] - i0;
-      float x[16];
-      if (!s_err) {
-        uint4 wa, wb;
-        lds_row_part(qst + row * kRowBytes, t, row & 1, wa, wb);
-        const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w}, xb[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          x[2 * j] = bf_lo(xa[j]) * a.qscale;
-          x[2 * j + 1] = bf_hi(xa[j]) * a.qscale;
-          x[8 + 2 * j] = bf_lo(xb[j]) * a.qscale;
-          x[8 + 2 * j + 1] = bf_hi(xb[j]) * a.qscale;
-        }
-      } else {
-#pragma unroll
-        for (int u = 0; u < 16; ++u) x[u] = 0.f;
-      }
-      const float2(&e)[8] = eq[h];
+  for (int h = 0; h < 2; ++h) {
+    const int row = ic[h] - i0;
+    float x[16];
+    if (!s_err) {
+      uint4 wa, wb;
+      lds_row_part(ring + row * kRowBytes, t, row & 1, wa, wb);
+      const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w}, xb[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        q1[h][j] = make_float2(x[2 * j], x[2 * j + 1]);
-        q2[h][j] = make_float2(x[8 + 2 * j], x[8 + 2 * j + 1]);
+        x[2 * j] = bf_lo(xa[j]) * a.qscale;
+        x[2 * j + 1] = bf_hi(xa[j]) * a.qscale;
+        x[8 + 2 * j] = bf_lo(xb[j]) * a.qscale;
+        x[8 + 2 * j + 1] = bf_hi(xb[j]) * a.qscale;
       }
-      float y[16];
+    } else {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        y[u] = x[u] * e[u].x - x[8 + u] * e[u].y;
-        y[8 + u] = x[u] * e[u].y + x[8 + u] * e[u].x;
-      }
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        qa[h][0][s] = pack_h2(y[2 * s], y[2 * s + 1]);
-        qa[h][1][s] = pack_h2(y[8 + 2 * s], y[8 + 2 * s + 1]);
-      }
+      for (int u = 0; u < 16; ++u) x[u] = 0.f;
     }
-  }
-  if (a.fac_dev != nullptr) {  // the factor tables rode in after the Q rows
-    const float* src = reinterpret_cast<const float*>(ring + kTcTile * kRowBytes);
-    for (int idx = tid; idx < nr * 64; idx += kConsumers) {
-      fac[idx] = src[idx];
-      if (MODE == 1) fac[a.fac_stride * 64 + idx] = src[nr * 64 + idx];
+    const float2(&e)[8] = eq[h];
+    float y[16];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      y[u] = x[u] * e[u].x - x[8 + u] * e[u].y;
+      y[8 + u] = x[u] * e[u].y + x[8 + u] * e[u].x;
+    }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      qa[h][0][s] = pack_h2(y[2 * s], y[2 * s + 1]);
+      qa[h][1][s] = pack_h2(y[8 + 2 * s], y[8 + 2 * s + 1]);
     }
   }
   release_stage(0);
 
-  // ---- stages 1, 2: window rows, converted in place: K -> K' f16 rotated (chunk c of row
-  // r at c ^ 4(r&1)), V -> f16 with columns in pi order (chunk ^ (r&7))
-  uint4* Ks = reinterpret_cast<uint4*>(ring + 1 * a.slot_bytes);
-  uint4* Vs = reinterpret_cast<uint4*>(ring + 2 * a.slot_bytes);
-  wait_stage(1);
-#pragma unroll
-  for (int k = 0; k < kKTasks; ++k) {
-    const int task = tid + k * kConsumers;
-    if (task >= kWinRows * 4) break;
-    const int row = task >> 2, c = task & 3;
-    const int p = i0 - 16 + row;
-    uint4 lo4 = make_uint4(0, 0, 0, 0), hi4 = make_uint4(0, 0, 0, 0);
-    if (p >= 0 && p < N && !s_err) {
-      const uint4 wa = Ks[row * 8 + c], wb = Ks[row * 8 + c + 4];
-      const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w}, xb[4] = {wb.x, wb.y, wb.z, wb.w};
-      const float2(&e)[8] = ek[k];
-      uint32_t ya[4], yb[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 k1 = bf2(xa[j]), k2 = bf2(xb[j]);
-        const float2 e0 = e[2 * j], e1 = e[2 * j + 1];
-        ya[j] = pack_h2(k1.x * e0.x - k2.x * e0.y, k1.y * e1.x - k2.y * e1.y);
-        yb[j] = pack_h2(k1.x * e0.y + k2.x * e0.x, k1.y * e1.y + k2.y * e1.x);
-      }
-      lo4 = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-      hi4 = make_uint4(yb[0], yb[1], yb[2], yb[3]);
-    }
-    const int sw = (row & 1) * 4;  // this thread read exactly chunks c and c+4 of this row
-    Ks[row * 8 + (c ^ sw)] = lo4;
-    Ks[row * 8 + ((c + 4) ^ sw)] = hi4;
-  }
-  wait_stage(2);
-  {
-    constexpr int kVTasks = kWinRows * 8 / kConsumers;  // 5 (4 warps) or 6 (2 warps)
-    static_assert(kVTasks * kConsumers == kWinRows * 8, "V conversion tasks must divide evenly");
-    uint32_t w[kVTasks][4];
-#pragma unroll
-    for (int k = 0; k < kVTasks; ++k) {
-      const int task = tid + k * kConsumers;
-      const int row = task >> 3, c8 = task & 7;
-      const int p = i0 - 16 + row;
-      w[k][0] = w[k][1] = w[k][2] = w[k][3] = 0u;
-      if (p >= 0 && p < N && !s_err) {
-        const uint4 raw = Vs[row * 8 + c8];
-        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) w[k][j] = pack_h2(bf_lo(rw[j]), bf_hi(rw[j]));
-      }
-    }
-    consumer_sync();  // every raw V chunk is in registers (and K' is complete)
-#pragma unroll
-    for (int k = 0; k < kVTasks; ++k) {
-      const int task = tid + k * kConsumers;
-      const int row = task >> 3, c8 = task & 7;
-      const int hh = c8 >> 2, tt = c8 & 3;
-      uint32_t* vrow = reinterpret_cast<uint32_t*>(Vs + row * 8);
-      // dim 32hh + 8tt + u  ->  column 8 (4hh + u/2) + 2tt + (u%2)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) vrow[((4 * hh + j) ^ (row & 7)) * 4 + tt] = w[k][j];
-    }
-    consumer_sync();
-  }
-
-  // ---- window: S = Q' K'^T over keys [q0-16, q0+16)
+  // ---- window: S = Q' K'^T over keys [q0-16, q0+16) (slot row r holds position i0-16+r;
+  // rows outside [w0, i_last] hold stale data: their scores are masked below)
+  const uint4* Ks = reinterpret_cast<const uint4*>(ring + 1 * a.slot_bytes);
+  const unsigned char* Vs = ring + 2 * a.slot_bytes;
   float S[4][4];
+  wait_stage(1);
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) S[nt][u] = 0.f;
     const int row = 16 * warp + 8 * nt + g;
-    const int sw = (row & 1) * 4;
-    const uint4 klo = Ks[row * 8 + (t ^ sw)];
-    const uint4 khi = Ks[row * 8 + ((t + 4) ^ sw)];
-    const uint32_t kl[4] = {klo.x, klo.y, klo.z, klo.w};
-    const uint32_t kh[4] = {khi.x, khi.y, khi.z, khi.w};
+    uint32_t kl[4], kh[4];
+    lds_kfrag(Ks + row * 8, t, i0 - 16 + row, kl, kh);
 #pragma unroll
     for (int s = 0; s < 4; ++s)
       mma16816(S[nt], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
@@ -535,119 +442,144 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
     lw[h] = sum;  // lane-partial window sum
     lr[h] = 0.f;  // rung sum (the same in the 4 lanes of a quad)
   }
-  // ---- window: O = P V
-  float2 O[8][2];  // [n-tile nd][row h] = dims (2nd, 2nd+1) of D_t
+  // ---- window: O = P V'.  ldmatrix lane l supplies row (l&7) of matrix l>>3: keys
+  // 16 s2 + 8 ((l>>3)&1) + (l&7), chunk nd + (l>>4).  Rows outside [w0, i_last] (P = 0 there)
+  // are read from the nearest copied row, so that no stale value can turn 0 * x into NaN.
+  float O[8][4];  // [n-tile nt]: (row g: dims 8nt+2t, +1), (row g+8: the same dims)
 #pragma unroll
-  for (int nd = 0; nd < 8; ++nd) O[nd][0] = O[nd][1] = make_float2(0.f, 0.f);
-  {
-    const int mi = lane >> 3, rl = lane & 7;
+  for (int nt = 0; nt < 8; ++nt) O[nt][0] = O[nt][1] = O[nt][2] = O[nt][3] = 0.f;
+  const int mi = lane >> 3, rl = lane & 7;
+  wait_stage(2);
 #pragma unroll
-    for (int s2 = 0; s2 < 2; ++s2) {
-      const uint32_t pa0 = pack_h2(S[2 * s2][0], S[2 * s2][1]);
-      const uint32_t pa1 = pack_h2(S[2 * s2][2], S[2 * s2][3]);
-      const uint32_t pa2 = pack_h2(S[2 * s2 + 1][0], S[2 * s2 + 1][1]);
-      const uint32_t pa3 = pack_h2(S[2 * s2 + 1][2], S[2 * s2 + 1][3]);
-      const int vrow = 16 * warp + 16 * s2 + (mi & 1) * 8 + rl;
+  for (int s2 = 0; s2 < 2; ++s2) {
+    const uint32_t pa0 = pack_h2(S[2 * s2][0], S[2 * s2][1]);
+    const uint32_t pa1 = pack_h2(S[2 * s2][2], S[2 * s2][3]);
+    const uint32_t pa2 = pack_h2(S[2 * s2 + 1][0], S[2 * s2 + 1][1]);
+    const uint32_t pa3 = pack_h2(S[2 * s2 + 1][2], S[2 * s2 + 1][3]);
+    const int pc = min(max(q0 - 16 + 16 * s2 + (mi & 1) * 8 + rl, w0), i_last);
+    const unsigned char* vrow = Vs + (pc - (i0 - 16)) * kRowBytes;
+    const int sw = swz(pc);
 #pragma unroll
-      for (int nd = 0; nd < 8; nd += 2) {
-        const int ch = (nd + (mi >> 1)) ^ (vrow & 7);
-        uint32_t b[4];
-        ldsm_x4_trans(b, Vs + vrow * 8 + ch);
-        float c0[4] = {O[nd][0].x, O[nd][0].y, O[nd][1].x, O[nd][1].y};
-        float c1[4] = {O[nd + 1][0].x, O[nd + 1][0].y, O[nd + 1][1].x, O[nd + 1][1].y};
-        mma16816(c0, pa0, pa1, pa2, pa3, b[0], b[1]);
-        mma16816(c1, pa0, pa1, pa2, pa3, b[2], b[3]);
-        O[nd][0] = make_float2(c0[0], c0[1]);
-        O[nd][1] = make_float2(c0[2], c0[3]);
-        O[nd + 1][0] = make_float2(c1[0], c1[1]);
-        O[nd + 1][1] = make_float2(c1[2], c1[3]);
-      }
+    for (int nd = 0; nd < 8; nd += 2) {
+      uint32_t b[4];
+      ldsm_x4_trans(b, vrow + ((nd + (mi >> 1)) ^ sw) * 16);
+      mma16816(O[nd], pa0, pa1, pa2, pa3, b[0], b[1]);
+      mma16816(O[nd + 1], pa0, pa1, pa2, pa3, b[2], b[3]);
     }
   }
   release_stage(2);
 
   // ---- rungs: chunks of kRungChunk, online softmax; rung r is stage 3 + r.
-  // The slab row of query i is i - i0 (+1 for interp) for every rung.  Inside a warp the
-  // arithmetic is branch-free: a row that does not attend the rung reads the slab's first
-  // copied row instead (finite data) and gets p = 0; a warp none of whose rows attends the
-  // rung skips it as a whole (a uniform branch).
+  // Slab row of query i: i - i0 + kI (global row i - lo; interp: its partner i - lo - 1 is
+  // the row before).  Rows that a query does not attend are read from the slab's first
+  // copied row (finite data) and get p = 0; a warp none of whose rows attends either rung
+  // of a chunk skips it as a whole (a uniform branch).
+  // Diagonal pick: query g's score sits in lane (g, g>>1) of key n-tile 0, element g&1; query
+  // g+8's in the same lane of n-tile 1, element 2 + (g&1).  That lane also holds the nonzero
+  // entries of A = diag(P): row g in a0, row g+8 in a3, each in half g&1.
+  const int src_lane = 4 * g + (g >> 1);
+  const float sel_lo = (t == (g >> 1) && !(g & 1)) ? 1.f : 0.f;
+  const float sel_hi = (t == (g >> 1) && (g & 1)) ? 1.f : 0.f;
+  const int lcop = i_last - i0 + kI;  // last copied slab row of every rung
   int srow[2];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) srow[h] = ic[h] - i0 + (MODE == 1 ? 1 : 0);
+  for (int h = 0; h < 2; ++h) srow[h] = ic[h] - i0 + kI;
   for (int r0 = 0; r0 < nrt; r0 += kRungChunk) {
 #pragma unroll
     for (int cc = 0; cc < kRungChunk; ++cc)
       if (r0 + cc < nrt) wait_stage(3 + r0 + cc);
     float sc[2][kRungChunk];
-    bool act[kRungChunk];
-    int rowu[2][kRungChunk], fcop[kRungChunk];
+    bool ok[2][kRungChunk], act[kRungChunk];
+    int rowu[2][kRungChunk], first[kRungChunk], fcop[kRungChunk];
 #pragma unroll
     for (int cc = 0; cc < kRungChunk; ++cc) {
-      const int r = r0 + cc < nrt ? r0 + cc : r0;
+      const int r = r0 + cc < nrt ? r0 + cc : r0;  // a chunk past the end repeats rung r0, masked
       const int c = W + r;
       const int lo = ks.lo[c];
       const bool in = (r0 + cc < nrt) && !s_err;
-      bool ok[2];
-      // first copied row of this slab (slab rows start at global row i0 - lo - interp)
-      const int first_copied = max(0, lo - i0 + (MODE == 1 ? 1 : 0));
-      fcop[cc] = first_copied;
+      first[cc] = i0 - lo - kI;             // global row of slab row 0
+      fcop[cc] = max(0, lo - i0 + kI);      // first copied slab row (<= lcop: the tile attends r)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        ok[h] = in && ic[h] >= ks.need[c];
-        rowu[h][cc] = ok[h] ? srow[h] : first_copied;
+        ok[h][cc] = in && ic[h] >= ks.need[c];
+        rowu[h][cc] = ok[h][cc] ? srow[h] : fcop[cc];
+        sc[h][cc] = -INFINITY;
       }
-      act[cc] = __any_sync(0xffffffffu, ok[0] || ok[1]);
-      sc[0][cc] = sc[1][cc] = -INFINITY;
-      if (act[cc]) {
-        const unsigned char* kst = ring + ((3 + r) % kSlots) * a.slot_bytes;
-        float2 cs[4], sn[4], ns[4];
-        load_fac(fac + r * 64, t, cs, sn);
+      act[cc] = __any_sync(0xffffffffu, ok[0][cc] || ok[1][cc]);
+    }
+    if (act[0] || act[1]) {  // uniform; the chunk's MMAs in one block, free to overlap
+      float C[kRungChunk][2][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) ns[j] = make_float2(-sn[j].x, -sn[j].y);
-        float part[2];
+      for (int cc = 0; cc < kRungChunk; ++cc) {
+        const int r = r0 + cc < nrt ? r0 + cc : r0;
+        const uint4* kst = reinterpret_cast<const uint4*>(ring + ((3 + r) % kSlots) * a.slot_bytes);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int row = rowu[h][cc];
-          uint4 ka, kb;
-          lds_row_part(kst + row * kRowBytes, t, row & 1, ka, kb);
-          part[h] = rung_dot(q1[h], q2[h], cs, sn, ns, ka, kb);
-        }
-        if (MODE == 1) {
-          const float w = ks.w[c];
-          if (w > 0.f) {  // uniform: w belongs to the rung
-            float2 c2[4], s2[4], n2[4];
-            load_fac(fac + (a.fac_stride + r) * 64, t, c2, s2);
+          uint32_t kl[4], kh[4];
+          lds_kfrag(kst + rowu[h][cc] * 8, t, first[cc] + rowu[h][cc], kl, kh);
+          C[cc][h][0] = C[cc][h][1] = C[cc][h][2] = C[cc][h][3] = 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) n2[j] = make_float2(-s2[j].x, -s2[j].y);
+          for (int s = 0; s < 4; ++s)
+            mma16816(C[cc][h], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
+        }
+      }
+#pragma unroll
+      for (int cc = 0; cc < kRungChunk; ++cc) {
+        float d0 = (g & 1) ? C[cc][0][1] : C[cc][0][0];
+        float d1 = (g & 1) ? C[cc][1][3] : C[cc][1][2];
+        if (MODE == 1) {
+          const int r = r0 + cc < nrt ? r0 + cc : r0;
+          const float w = ks.w[W + r];
+          if (w > 0.f) {  // uniform: w belongs to the rung
+            const uint4* kst = reinterpret_cast<const uint4*>(ring + ((3 + r) % kSlots) * a.slot_bytes);
+            float C2[2][4];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const int row = max(rowu[h][cc] - 1, first_copied);
-              uint4 ka, kb;
-              lds_row_part(kst + row * kRowBytes, t, row & 1, ka, kb);
-              part[h] = (1.f - w) * part[h] + w * rung_dot(q1[h], q2[h], c2, s2, n2, ka, kb);
+              const int row = max(rowu[h][cc] - 1, fcop[cc]);
+              uint32_t kl[4], kh[4];
+              lds_kfrag(kst + row * 8, t, first[cc] + row, kl, kh);
+              C2[h][0] = C2[h][1] = C2[h][2] = C2[h][3] = 0.f;
+#pragma unroll
+              for (int s = 0; s < 4; ++s)
+                mma16816(C2[h], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
             }
+            d0 = (1.f - w) * d0 + w * ((g & 1) ? C2[0][1] : C2[0][0]);
+            d1 = (1.f - w) * d1 + w * ((g & 1) ? C2[1][3] : C2[1][2]);
           }
         }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          part[h] += __shfl_xor_sync(0xffffffffu, part[h], 1);
-          part[h] += __shfl_xor_sync(0xffffffffu, part[h], 2);
-          sc[h][cc] = ok[h] ? part[h] : -INFINITY;
-        }
+        d0 = __shfl_sync(0xffffffffu, d0, src_lane);
+        d1 = __shfl_sync(0xffffffffu, d1, src_lane);
+        sc[0][cc] = ok[0][cc] ? d0 : -INFINITY;
+        sc[1][cc] = ok[1][cc] ? d1 : -INFINITY;
       }
     }
+    // Online softmax with a lazy reference: m only moves when a score passes it by more
+    // than 8 (log2 units), so p = 2^(s - m) <= 256 (exact in f16 range) and O and the sums
+    // are rescaled only then.
+    bool grow = false;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float mc = m[h];
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int cc = 0; cc < kRungChunk; ++cc) mc = fmaxf(mc, sc[h][cc]);
-      const float corr = exp2f(m[h] - mc);
-      m[h] = mc;
-      lw[h] *= corr;
-      lr[h] *= corr;
-      const float2 corr2 = make_float2(corr, corr);
+      for (int cc = 0; cc < kRungChunk; ++cc) grow |= sc[h][cc] > m[h] + 8.f;
+    if (__any_sync(0xffffffffu, grow)) {  // uniform
+      float corr[2];
 #pragma unroll
-      for (int nd = 0; nd < 8; ++nd) O[nd][h] = __fmul2_rn(O[nd][h], corr2);
+      for (int h = 0; h < 2; ++h) {
+        float mc = m[h];
+#pragma unroll
+        for (int cc = 0; cc < kRungChunk; ++cc) mc = fmaxf(mc, sc[h][cc]);
+        corr[h] = exp2f(m[h] - mc);
+        m[h] = mc;
+        lw[h] *= corr[h];
+        lr[h] *= corr[h];
+      }
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        O[nt][0] *= corr[0];
+        O[nt][1] *= corr[0];
+        O[nt][2] *= corr[1];
+        O[nt][3] *= corr[1];
+      }
     }
 #pragma unroll
     for (int cc = 0; cc < kRungChunk; ++cc) {
@@ -655,31 +587,29 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
       const int r = r0 + cc;
       const float w = MODE == 1 ? ks.w[W + r] : 0.f;
       const unsigned char* vst = ring + ((3 + r) % kSlots) * a.slot_bytes + SR * kRowBytes;
+      float p[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const float p = exp2f(sc[h][cc] - m[h]);  // 0 for a row that does not attend
-        lr[h] += p;
-        const int row = rowu[h][cc];
-        uint4 va, vb;
-        lds_row_part(vst + row * kRowBytes, t, row & 1, va, vb);
-        const uint32_t xa[4] = {va.x, va.y, va.z, va.w}, xb[4] = {vb.x, vb.y, vb.z, vb.w};
-        const float p0 = p * (1.f - w);
-        const float2 pp = make_float2(p0, p0);
+        p[h] = exp2f(sc[h][cc] - m[h]);  // 0 for a row that does not attend
+        lr[h] += p[h];
+      }
+      // O += diag(p (1-w)) V'[slab rows of the 16 queries]; interp: + diag(p w) V'[rows - 1]
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          O[j][h] = __ffma2_rn(pp, bf2(xa[j]), O[j][h]);
-          O[4 + j][h] = __ffma2_rn(pp, bf2(xb[j]), O[4 + j][h]);
-        }
-        if (MODE == 1 && w > 0.f) {
-          const int row1 = max(row - 1, fcop[cc]);
-          lds_row_part(vst + row1 * kRowBytes, t, row1 & 1, va, vb);
-          const uint32_t ya[4] = {va.x, va.y, va.z, va.w}, yb[4] = {vb.x, vb.y, vb.z, vb.w};
-          const float2 pw = make_float2(p * w, p * w);
+      for (int part = 0; part < (MODE == 1 ? 2 : 1); ++part) {
+        if (part == 1 && !(w > 0.f)) break;  // uniform
+        const float f = MODE == 1 ? (part == 0 ? 1.f - w : w) : 1.f;
+        const float x0 = p[0] * f, x1 = p[1] * f;
+        const uint32_t a0 = pack_h2(x0 * sel_lo, x0 * sel_hi);
+        const uint32_t a3 = pack_h2(x1 * sel_lo, x1 * sel_hi);
+        const int vr = min(max(16 * warp + (mi & 1) * 8 + rl + kI - part, fcop[cc]), lcop);
+        const unsigned char* vrow = vst + vr * kRowBytes;
+        const int sw = swz(first[cc] + vr);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            O[j][h] = __ffma2_rn(pw, bf2(ya[j]), O[j][h]);
-            O[4 + j][h] = __ffma2_rn(pw, bf2(yb[j]), O[4 + j][h]);
-          }
+        for (int nd = 0; nd < 8; nd += 2) {
+          uint32_t b[4];
+          ldsm_x4_trans(b, vrow + ((nd + (mi >> 1)) ^ sw) * 16);
+          mma16816(O[nd], a0, 0u, 0u, a3, b[0], b[1]);
+          mma16816(O[nd + 1], a0, 0u, 0u, a3, b[2], b[3]);
         }
       }
     }
@@ -699,15 +629,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
     const int i = irow[h];
     if (i < N) {
       const float inv = 1.f / l;
-      float ov[16];
+      uint32_t* orow = reinterpret_cast<uint32_t*>(a.o + base + static_cast<size_t>(i) * kD);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        ov[2 * j] = O[j][h].x * inv;
-        ov[2 * j + 1] = O[j][h].y * inv;
-        ov[8 + 2 * j] = O[4 + j][h].x * inv;
-        ov[8 + 2 * j + 1] = O[4 + j][h].y * inv;
-      }
-      store_part(a.o + base + static_cast<size_t>(i) * kD, t, ov);
+      for (int nt = 0; nt < 8; ++nt)
+        orow[4 * nt + t] = pack_bf2_rn(O[nt][2 * h] * inv, O[nt][2 * h + 1] * inv);
       if (t == 0 && a.lse != nullptr) a.lse[static_cast<size_t>(bh) * N + i] = (m[h] + log2f(l)) * kLn2;
     }
   }
@@ -715,25 +640,33 @@ __global__ void __launch_bounds__(kTcThreads, kTcWarps == 4 ? (MODE == 0 ? 3 : 2
 
 bool tc_supported(const LayerTable& t) { return t.W <= kTcMaxW; }
 
+size_t fwd_tc_workspace_bytes(int B, int H, int N) {
+  return static_cast<size_t>(B) * H * N * kD * 2 * sizeof(__half);
+}
+
 cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k,
                           const void* v, void* o, float* lse, const float2* lo_tab,
                           const float2* hi_tab, int* status, unsigned long long wait_ns,
-                          int skip_first_rung_copy, const float* fac_dev, cudaStream_t stream) {
+                          int skip_first_rung_copy, void* workspace, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(B) * H * N;
+  __half* kp = static_cast<__half*>(workspace);
+  __half* vp = kp + rows * kD;
+  const long long prep_blocks = (rows * 4 + 255) / 256;
+  if (prep_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  prep_kv_kernel<<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), kp, vp, lo_tab, hi_tab, N,
+      rows);
+
   TcArgs a;
-  // the Q rows (8 KB) and the factor tables (256 B per rung, two tables for interp) share a slot
-  const int slot = 2 * (t.mode == 1 ? kTcTile + 8 : kTcTile) * kRowBytes;
-  const bool fits = kTcTile * kRowBytes + (t.mode == 1 ? 2 : 1) * t.n * 256 <= slot;
-  a.fac_dev = fits ? fac_dev : nullptr;
   a.t = t;
   a.N = N;
   a.tiles = (N + kTcTile - 1) / kTcTile;
   a.bh = B * H;
   a.slab_rows = t.mode == 1 ? kTcTile + 8 : kTcTile;
   a.slot_bytes = 2 * a.slab_rows * kRowBytes;
-  a.fac_stride = t.n > 0 ? t.n : 1;  // rungs kept <= t.n (device-alpha interp may keep fewer)
   a.q = static_cast<const __nv_bfloat16*>(q);
-  a.k = static_cast<const __nv_bfloat16*>(k);
-  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.kp = kp;
+  a.vp = vp;
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
   a.rope_lo = lo_tab;
@@ -744,20 +677,14 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   a.skip_first_rung_copy = skip_first_rung_copy;
   const long long blocks = static_cast<long long>(a.tiles) * B * H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const size_t smem = static_cast<size_t>(kSlots) * a.slot_bytes +
-                      static_cast<size_t>(t.mode == 1 ? 2 : 1) * a.fac_stride * 64 * sizeof(float);
-  // The opt-in limit is a property of the kernel function, not of a launch: launches that a
-  // CUDA graph captured earlier replay under whatever limit was set last.  So it is always
-  // set to the largest size any launch of this kernel can ask for (all kMaxR rungs).
-  const int smem_max = kSlots * 2 * (t.mode == 1 ? kTcTile + 8 : kTcTile) * kRowBytes +
-                       (t.mode == 1 ? 2 : 1) * kMaxR * 64 * static_cast<int>(sizeof(float));
+  const int smem = kSlots * a.slot_bytes;
   cudaError_t e;
   if (t.mode == 0) {
-    e = cudaFuncSetAttribute(fwd_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    e = cudaFuncSetAttribute(fwd_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     fwd_tc_kernel<0><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a);
   } else {
-    e = cudaFuncSetAttribute(fwd_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    e = cudaFuncSetAttribute(fwd_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     fwd_tc_kernel<1><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a);
   }

@@ -26,7 +26,7 @@ FIB_HEAD_DIM, FIB_MAX_RUNGS, FIB_MAX_WINDOW, FIB_MAX_LAYERS = 64, 32, 64, 256
 EXPORTS = [
     "fib_attn_error_string", "fib_attn_base", "fib_attn_schedule", "fib_attn_mask_distances",
     "fib_attn_interp_rungs", "fib_attn_plan_create", "fib_attn_plan_destroy",
-    "fib_attn_plan_distances", "fib_attn_fwd", "fib_attn_bwd_workspace_size", "fib_attn_bwd",
+    "fib_attn_plan_distances", "fib_attn_fwd_workspace_size", "fib_attn_fwd", "fib_attn_bwd_workspace_size", "fib_attn_bwd",
     "fib_attn_debug_indices", "fib_attn_last_device_status", "fib_attn_plan_set_debug",
     "fib_attn_bwd_noalloc", "fib_attn_decode",
 ]
@@ -48,7 +48,9 @@ _SIGS = {
                                   ctypes.c_double]),
     "fib_attn_plan_destroy": (_i, [_vp]),
     "fib_attn_plan_distances": (_i, [_vp, _i, _i, _i32p, _i, ctypes.POINTER(_i)]),
-    "fib_attn_fwd": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "fib_attn_fwd_workspace_size": (ctypes.c_size_t, [_vp, _i, _i, _i, _i]),
+    "fib_attn_fwd": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                          _vp]),
     "fib_attn_bwd_workspace_size": (ctypes.c_size_t, [_vp, _i, _i, _i]),
     "fib_attn_bwd": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                           _vp, _vp, ctypes.c_size_t, _vp]),
@@ -201,18 +203,26 @@ def _same(q, *ts):
             raise ValueError("q/k/v/o/dO/dq/dk/dv must share shape, dtype and be contiguous CUDA")
 
 
+def fib_attn_fwd_workspace_size(plan: Plan, B: int, H: int, N: int, dtype) -> int:
+    return int(lib().fib_attn_fwd_workspace_size(plan.handle, B, H, N, _DT.get(dtype, dtype)))
+
+
 def fib_attn_fwd(plan: Plan, layer: int, q, k, v, o=None, lse=None, alpha_dev=None,
-                 want_lse: bool = True, stream=None):
-    """Returns (o, lse).  o/lse are allocated (by torch) when not given."""
+                 want_lse: bool = True, workspace=None, stream=None):
+    """Returns (o, lse).  o/lse and the workspace are allocated (by torch) when not given."""
     B, H, N = _shape(q)
     _same(q, k, v, o)
     if o is None:
         o = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    need = fib_attn_fwd_workspace_size(plan, B, H, N, q.dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("fib_attn_fwd", lib().fib_attn_fwd(
         plan.handle, layer, B, H, N, _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-        _ptr(alpha_dev), _stream(stream)))
+        _ptr(alpha_dev), _ptr(workspace), ws_bytes, _stream(stream)))
     return o, lse
 
 

@@ -128,10 +128,18 @@ int fib_attn_plan_distances(fib_attn_plan_t p, int layer, int N, int32_t* out, i
  * NULL to skip writing it.  alpha_dev (INTERP only): device float32 alpha[n_layers]
  * (a learned parameter; element `layer` is used, exactly as a float32) or NULL to use
  * the plan's binary64 alpha.  MASK ignores alpha_dev.  O must not alias q, k or v.
- * Errors: FIB_ERR_INVALID_ARG (null/misaligned pointers, sizes, layer), FIB_ERR_CUDA.  */
+ * workspace: device scratch of at least fib_attn_fwd_workspace_size(p, B, H, N, dtype)
+ * bytes, 256-byte aligned, caller-owned, not overlapping q, k, v or o; its contents on
+ * entry are ignored and on return are unspecified.  bf16 with W <= 16 needs B*H*N*256
+ * bytes: the keys rotated to their own positions and the values, both as float16, which
+ * the tensor-core kernel reads instead of k and v.  Where the size is 0 (float32, or a
+ * window wider than 16), workspace may be NULL.
+ * Errors: FIB_ERR_INVALID_ARG (null/misaligned pointers, sizes, layer, a short or
+ * misaligned workspace), FIB_ERR_CUDA.                                                  */
+size_t fib_attn_fwd_workspace_size(fib_attn_plan_t p, int B, int H, int N, int dtype);
 int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
                  const void* q, const void* k, const void* v, void* o, float* lse,
-                 const float* alpha_dev, void* stream);
+                 const float* alpha_dev, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ decode ----
  * One new token per (b, h) against a KV cache (Key results 2, "Efficiency": inference

@@ -272,9 +272,9 @@ def test_device_error_paths():
     o = torch.empty_like(q)
     s = torch.cuda.current_stream().cuda_stream
 
-    def fwd(layer=0, n=N, dtype=0, qp=None, op=None, lsep=None):
+    def fwd(layer=0, n=N, dtype=0, qp=None, op=None, lsep=None, wsp=None, ws_bytes=0):
         return lib.fib_attn_fwd(plan.handle, layer, B, H, n, dtype, qp or q.data_ptr(), q.data_ptr(),
-                                q.data_ptr(), op or o.data_ptr(), lsep, None, s)
+                                q.data_ptr(), op or o.data_ptr(), lsep, None, wsp, ws_bytes, s)
 
     assert fwd() == fa.FIB_OK
     assert fwd(layer=2) == fa.FIB_ERR_INVALID_ARG            # layer out of range
@@ -285,6 +285,17 @@ def test_device_error_paths():
     assert fwd(qp=q.data_ptr() + 4) == fa.FIB_ERR_INVALID_ARG   # misaligned
     assert fwd(op=q.data_ptr()) == fa.FIB_ERR_INVALID_ARG       # o aliases q
     assert fwd(lsep=q.data_ptr() + 2) == fa.FIB_ERR_INVALID_ARG
+    # bf16 needs the K'/V' workspace: null, short, misaligned or aliasing an input is refused
+    assert fa.fib_attn_fwd_workspace_size(plan, B, H, N, torch.float32) == 0
+    fneed = fa.fib_attn_fwd_workspace_size(plan, B, H, N, torch.bfloat16)
+    assert fneed == B * H * N * 256
+    fws = torch.empty(fneed + 256, dtype=torch.uint8, device="cuda")
+    bf = fa.FIB_DTYPE_BF16
+    assert fwd(dtype=bf) == fa.FIB_ERR_INVALID_ARG
+    assert fwd(dtype=bf, wsp=fws.data_ptr(), ws_bytes=fneed - 1) == fa.FIB_ERR_INVALID_ARG
+    assert fwd(dtype=bf, wsp=fws.data_ptr() + 16, ws_bytes=fneed) == fa.FIB_ERR_INVALID_ARG
+    assert fwd(dtype=bf, wsp=q.data_ptr(), ws_bytes=fneed) == fa.FIB_ERR_INVALID_ARG
+    assert fwd(dtype=bf, wsp=fws.data_ptr(), ws_bytes=fneed) == fa.FIB_OK
     ws_need = fa.fib_attn_bwd_workspace_size(plan, B, H, N)
     ws = torch.empty(ws_need, dtype=torch.uint8, device="cuda")
     lse = torch.empty(B, H, N, device="cuda")

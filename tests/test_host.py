@@ -134,6 +134,8 @@ def test_plan_create_rejects_bad_arguments_before_any_device_call():
     assert call(a=(ctypes.c_double * 2)(1.0, -1.0)) == fa.FIB_ERR_INVALID_ARG
     assert lib.fib_attn_plan_create(None, 0, None, 0, a, 2, 12, 1024, 64, 0, 10000.0) == fa.FIB_ERR_INVALID_ARG
     assert lib.fib_attn_plan_destroy(None) == fa.FIB_OK
-    assert lib.fib_attn_fwd(None, 0, 1, 1, 1, 0, None, None, None, None, None, None, None) == fa.FIB_ERR_INVALID_ARG
+    assert lib.fib_attn_fwd(None, 0, 1, 1, 1, 0, None, None, None, None, None, None, None, 0,
+                            None) == fa.FIB_ERR_INVALID_ARG
+    assert lib.fib_attn_fwd_workspace_size(None, 1, 1, 1, fa.FIB_DTYPE_BF16) == 0
     assert lib.fib_attn_last_device_status(None) == fa.FIB_ERR_INVALID_ARG
     assert lib.fib_attn_bwd_workspace_size(None, 1, 1, 1) == 0
