@@ -168,25 +168,74 @@ def setup(w, device):
     adev = None
     if w["mode"] == "interp":
         adev = torch.tensor(alphas, dtype=torch.float32, device=device)
-    return plan, host, dev, outs, lses, adev
+    # one forward workspace per layer (prepared K/V), so that timing one half alone still
+    # reads every layer's own data
+    need = fa.fib_attn_fwd_workspace_size(plan, w["B"], w["H"], w["N"], dev[0][0].dtype)
+    wss = [torch.empty(need, dtype=torch.uint8, device=device) if need else None for _ in dev]
+    return plan, host, dev, outs, lses, adev, wss
 
 
-def run_stack(fa, plan, dev, outs, lses, adev):
+def run_stack(fa, plan, dev, outs, lses, adev, wss):
     for l, (q, k, v) in enumerate(dev):
-        fa.fib_attn_fwd(plan, l, q, k, v, o=outs[l], lse=lses[l], alpha_dev=adev)
+        fa.fib_attn_fwd(plan, l, q, k, v, o=outs[l], lse=lses[l], alpha_dev=adev, workspace=wss[l])
+
+
+def kernels_per_layer(wss):
+    return 2 if wss[0] is not None else 1
+
+
+def time_graph(torch, stream, device, fn, steps, warmup):
+    """Milliseconds per replay of a CUDA graph of fn(), CUDA events on `stream`."""
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        fn()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    return e0.elapsed_time(e1) / steps
+
+
+def time_halves(fa, torch, stream, device, plan, dev, outs, lses, adev, wss, steps, warmup):
+    """Per-launch device time of each kernel of the bf16 forward, each timed alone: a graph
+    of the L layers' attention launches (every layer's own prepared K/V, Q and O) and one
+    of the L preparation launches."""
+    if wss[0] is None:
+        return None
+    L = len(dev)
+
+    def attend():
+        for l, (q, _, _) in enumerate(dev):
+            fa.fib_attn_fwd_attend(plan, l, q, wss[l], o=outs[l], lse=lses[l], alpha_dev=adev)
+
+    def prepare():
+        for l, (_, k, v) in enumerate(dev):
+            fa.fib_attn_fwd_prepare_kv(plan, k, v, workspace=wss[l])
+
+    with torch.cuda.stream(stream):
+        prepare()
+    t_att = time_graph(torch, stream, device, attend, steps, warmup) / L
+    t_prep = time_graph(torch, stream, device, prepare, steps, warmup) / L
+    return {"attend_ms": t_att, "prepare_ms": t_prep}
 
 
 def time_device(w, steps, warmup, device, rank, world):
     import torch
     from fibonacci_offset_sparse_gb300 import fib_attn as fa
-    plan, host, dev, outs, lses, adev = setup(w, device)
+    plan, host, dev, outs, lses, adev, wss = setup(w, device)
     stream = torch.cuda.Stream(device)
     with torch.cuda.stream(stream):
-        run_stack(fa, plan, dev, outs, lses, adev)  # first call outside capture
+        run_stack(fa, plan, dev, outs, lses, adev, wss)  # first call outside capture
     torch.cuda.synchronize(device)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        run_stack(fa, plan, dev, outs, lses, adev)
+        run_stack(fa, plan, dev, outs, lses, adev, wss)
     for _ in range(warmup):
         graph.replay()
     torch.cuda.synchronize(device)
@@ -205,7 +254,8 @@ def time_device(w, steps, warmup, device, rank, world):
         t = torch.tensor([ms], device=device)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
-    res = dict(ms_total=ms, ms_per_step=ms / steps, launches=w["L"] * steps, clocks=clk.summary())
+    kpl = kernels_per_layer(wss)
+    res = dict(ms_total=ms, ms_per_step=ms / steps, launches=kpl * w["L"] * steps, clocks=clk.summary())
     # end to end through the public API: pinned host inputs -> device -> 16 layers -> host O
     pinned = [tuple(t.pin_memory() for t in layer) for layer in host]
     o_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
@@ -218,7 +268,7 @@ def time_device(w, steps, warmup, device, rank, world):
             dev[l][0].copy_(q, non_blocking=True)
             dev[l][1].copy_(k, non_blocking=True)
             dev[l][2].copy_(v, non_blocking=True)
-        run_stack(fa, plan, dev, outs, lses, adev)
+        run_stack(fa, plan, dev, outs, lses, adev, wss)
         for l in range(len(outs)):
             o_host[l].copy_(outs[l], non_blocking=True)
 
@@ -236,7 +286,8 @@ def time_device(w, steps, warmup, device, rank, world):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_e2e = float(t.item())
     res.update(ms_e2e_per_step=ms_e2e / e2e_steps, h2d=h2d, d2h=d2h, e2e_steps=e2e_steps,
-               e2e_launches=w["L"] * e2e_steps)
+               e2e_launches=kpl * w["L"] * e2e_steps)
+    res["halves"] = time_halves(fa, torch, stream, device, plan, dev, outs, lses, adev, wss, steps, warmup)
     plan.close()
     return res
 
@@ -350,7 +401,10 @@ def main():
     value = tokens_step * world / (r["ms_per_step"] / 1e3)
     e2e_value = tokens_step * world / (r["ms_e2e_per_step"] / 1e3)
     peak, peak_kind = read_peaks()
-    launch_s = r["ms_per_step"] / 1e3 / w["L"]
+    layer_s = r["ms_per_step"] / 1e3 / w["L"]
+    # dominant kernel: the attention launch, timed alone (its algorithmic bytes are the
+    # layer's compulsory bytes: Q and the prepared K, V read once, O written once)
+    launch_s = r["halves"]["attend_ms"] / 1e3 if r["halves"] else layer_s
     algo = compulsory_bytes(w)
     achieved = algo / launch_s / 1e9
     traffic = ncu_traffic(args.workload)
@@ -364,7 +418,13 @@ def main():
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_kind": peak_kind + (" (hbm_gbs, burst copy)" if peak_kind == "measured" else ""),
                      "algorithmic_bytes_per_launch": algo,
-                     "avg_launch_us": launch_s * 1e6},
+                     "avg_launch_us": launch_s * 1e6,
+                     "kernel": "fwd_tc_kernel (attention, prepared K/V)" if r["halves"] else "fwd_kernel"},
+        "layer": {"us_per_layer": layer_s * 1e6,
+                  "prepare_us_per_launch": r["halves"]["prepare_ms"] * 1e3 if r["halves"] else None,
+                  "attend_us_per_launch": r["halves"]["attend_ms"] * 1e3 if r["halves"] else None,
+                  "achieved_gbs": algo / layer_s / 1e9, "frac": algo / layer_s / 1e9 / peak,
+                  "note": "compulsory bytes of a layer over its whole forward (both kernels)"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "steps": r["e2e_steps"], "gpu_launches": r["e2e_launches"]},
         "gpu_launches": r["launches"],
@@ -376,10 +436,14 @@ def main():
             ws = WORKLOADS[name]
             rs = time_device(ws, args.steps, args.warmup, device, rank, world)
             ls = rs["ms_per_step"] / 1e3 / ws["L"]
-            ach = compulsory_bytes(ws) / ls / 1e9
+            la = rs["halves"]["attend_ms"] / 1e3 if rs["halves"] else ls
+            ach = compulsory_bytes(ws) / la / 1e9
             sec[name] = {"value": ws["B"] * ws["N"] * world / (rs["ms_per_step"] / 1e3), "unit": UNIT,
-                         "ms_per_step": rs["ms_per_step"], "avg_launch_us": ls * 1e6,
-                         "achieved_gbs": ach, "frac": ach / peak, "traffic": ncu_traffic(name)}
+                         "ms_per_step": rs["ms_per_step"], "us_per_layer": ls * 1e6,
+                         "attend_us_per_launch": la * 1e6,
+                         "prepare_us_per_launch": rs["halves"]["prepare_ms"] * 1e3 if rs["halves"] else None,
+                         "achieved_gbs": ach, "frac": ach / peak,
+                         "layer_frac": compulsory_bytes(ws) / ls / 1e9 / peak, "traffic": ncu_traffic(name)}
         line["secondary"] = sec
     try:
         dense = {}

@@ -21,10 +21,11 @@ cudaError_t launch_fwd(const LayerTable& t, int B, int H, int N, int dtype, cons
                        const float2* hi_tab, cudaStream_t stream);
 bool tc_supported(const LayerTable& t);
 size_t fwd_tc_workspace_bytes(int B, int H, int N);
-cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k,
-                          const void* v, void* o, float* lse, const float2* lo_tab,
-                          const float2* hi_tab, int* status, unsigned long long wait_ns,
-                          int skip_first_rung_copy, void* workspace, cudaStream_t stream);
+cudaError_t launch_prep_kv(int B, int H, int N, const void* k, const void* v, const float2* lo_tab,
+                           const float2* hi_tab, void* workspace, cudaStream_t stream);
+cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* workspace,
+                          void* o, float* lse, const float2* lo_tab, const float2* hi_tab, int* status,
+                          unsigned long long wait_ns, int skip_first_rung_copy, cudaStream_t stream);
 cudaError_t launch_debug_indices(const LayerTable& t, int N, int i0, int i1, int32_t* out,
                                  float* w_out, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int H, int N);
@@ -316,12 +317,52 @@ int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, c
   if (st != FIB_OK) return st;
   // bf16 with a window of at most 16 keys: K'/V' preparation plus the tensor-core kernel
   // (fwd_tc.cu); otherwise the CUDA-core kernel (fwd.cu), which also serves float32 exactly.
-  if (dtype == FIB_DTYPE_BF16 && tc_supported(t))
-    return cuda_status(launch_fwd_tc(t, B, H, N, q, k, v, o, lse, p->d_lo, p->d_hi, p->d_status,
-                                     p->wait_ns, p->skip_first_rung_copy, workspace,
-                                     static_cast<cudaStream_t>(stream)));
+  if (dtype == FIB_DTYPE_BF16 && tc_supported(t)) {
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = launch_prep_kv(B, H, N, k, v, p->d_lo, p->d_hi, workspace, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    return cuda_status(launch_fwd_tc(t, B, H, N, q, workspace, o, lse, p->d_lo, p->d_hi, p->d_status,
+                                     p->wait_ns, p->skip_first_rung_copy, s));
+  }
   return cuda_status(launch_fwd(t, B, H, N, dtype, q, k, v, o, lse, p->d_lo, p->d_hi,
                                 static_cast<cudaStream_t>(stream)));
+}
+
+int fib_attn_fwd_prepare_kv(fib_attn_plan_t p, int B, int H, int N, int dtype, const void* k,
+                            const void* v, void* workspace, size_t ws_bytes, void* stream) {
+  int st = check_shape(p, 0, B, H, N, dtype);
+  if (st != FIB_OK) return st;
+  const size_t need = fib_attn_fwd_workspace_size(p, B, H, N, dtype);
+  if (need == 0) return FIB_ERR_UNSUPPORTED;
+  if (check_tensor(k) || check_tensor(v)) return FIB_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < need) return FIB_ERR_INVALID_ARG;
+  if (workspace == k || workspace == v) return FIB_ERR_INVALID_ARG;
+  st = check_device(p);
+  if (st != FIB_OK) return st;
+  return cuda_status(launch_prep_kv(B, H, N, k, v, p->d_lo, p->d_hi, workspace,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+int fib_attn_fwd_attend(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, const void* q,
+                        const void* workspace, size_t ws_bytes, void* o, float* lse,
+                        const float* alpha_dev, void* stream) {
+  int st = check_shape(p, layer, B, H, N, dtype);
+  if (st != FIB_OK) return st;
+  const size_t need = fib_attn_fwd_workspace_size(p, B, H, N, dtype);
+  if (need == 0) return FIB_ERR_UNSUPPORTED;
+  if (check_tensor(q) || check_tensor(o) || o == q) return FIB_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < need) return FIB_ERR_INVALID_ARG;
+  if (workspace == q || workspace == o) return FIB_ERR_INVALID_ARG;
+  if (lse != nullptr && !aligned(lse, 4)) return FIB_ERR_INVALID_ARG;
+  if (alpha_dev != nullptr && !aligned(alpha_dev, 4)) return FIB_ERR_INVALID_ARG;
+  st = check_device(p);
+  if (st != FIB_OK) return st;
+  LayerTable t;
+  st = make_table(p, layer, N, p->mode == FIB_MODE_INTERP ? alpha_dev : nullptr, &t);
+  if (st != FIB_OK) return st;
+  return cuda_status(launch_fwd_tc(t, B, H, N, q, workspace, o, lse, p->d_lo, p->d_hi, p->d_status,
+                                   p->wait_ns, p->skip_first_rung_copy,
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 int fib_attn_decode(fib_attn_plan_t p, int layer, int B, int H, int N, int pos, int dtype,

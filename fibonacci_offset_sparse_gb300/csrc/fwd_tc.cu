@@ -12,10 +12,12 @@
 //     queries plus one producer thread that streams the rows they read through a 3-slot
 //     shared-memory ring with cp.async.bulk (mbarrier completion): the Q rows, the window
 //     rows [i0-16, i0+64) of K' and V', then per rung the slab rows [i0-d, i0-d+64) of K'
-//     and V'.  The producer runs up to 3 slots ahead and refills a slot once the 4 compute
-//     warps release it (3 slots of 16 KB and 96 registers a thread let 4 CTAs share an SM).  Every mbarrier wait is bounded in time; a wait that gives up
-//     records FIB_ERR_TIMEOUT in the plan's status word, the warps stop, and the producer
-//     lets its copies in flight land before the CTA exits.
+//     and V'.  The producer refills a slot once the 4 compute warps release it; with one
+//     rung per online-softmax step the next two stages are in flight while a rung is being
+//     computed.  3 slots of 16 KB and 96 registers a thread let 4 CTAs share an SM.  Every
+//     mbarrier wait is bounded in time; a wait that gives up records FIB_ERR_TIMEOUT in the
+//     plan's status word, the warps stop, and the producer lets its copies in flight land
+//     before the CTA exits.
 //   * window band: for a warp's 16 queries every window key lies in the 32-row block
 //     [q0-16, q0+16) (W <= 16): S = Q' K'^T and O = P V' as mma.sync m16n8k16 (f16
 //     operands, f32 accumulation), Q' rotated at its own position and scaled by
@@ -46,8 +48,17 @@ constexpr int kTcTile = 16 * kTcWarps;         // queries per CTA
 constexpr int kConsumers = 32 * kTcWarps;
 constexpr int kTcThreads = kConsumers + 32;    // + one producer warp
 constexpr int kTcMaxW = 16;
-constexpr int kSlots = 3;                      // ring slots
-constexpr int kRungChunk = 2;                  // rungs per online-softmax step
+#ifndef FIB_TC_SLOTS
+#define FIB_TC_SLOTS 3
+#endif
+#ifndef FIB_TC_CHUNK
+#define FIB_TC_CHUNK 1
+#endif
+#ifndef FIB_TC_MIN_CTAS
+#define FIB_TC_MIN_CTAS 4
+#endif
+constexpr int kSlots = FIB_TC_SLOTS;           // ring slots
+constexpr int kRungChunk = FIB_TC_CHUNK;       // rungs per online-softmax step
 constexpr int kRowBytes = kD * 2;              // one row of 16-bit values
 
 struct TcArgs {
@@ -211,38 +222,38 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const __nv_bfloat16* __res
   const int p = static_cast<int>(row % N);
   const uint4* k4 = reinterpret_cast<const uint4*>(k + row * kD);
   const uint4* v4 = reinterpret_cast<const uint4*>(v + row * kD);
-  const uint4 ka = __ldg(k4 + u), kb = __ldg(k4 + u + 4), va = __ldg(v4 + u), vb = __ldg(v4 + u + 4);
+  const uint4 ka = __ldcs(k4 + u), kb = __ldcs(k4 + u + 4), va = __ldcs(v4 + u), vb = __ldcs(v4 + u + 4);
   float2 e[8];
   rope_row(lo_tab, hi_tab, p, u, e);
   const uint32_t xa[4] = {ka.x, ka.y, ka.z, ka.w}, xb[4] = {kb.x, kb.y, kb.z, kb.w};
   uint32_t ya[4], yb[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    // (k_m, k_{m+32}) -> (k_m c - k_{m+32} s, k_m s + k_{m+32} c), m = 8u + 2j (+1)
-    const float k1x = bf_lo(xa[j]), k1y = bf_hi(xa[j]), k2x = bf_lo(xb[j]), k2y = bf_hi(xb[j]);
-    const float2 e0 = e[2 * j], e1 = e[2 * j + 1];
-    ya[j] = pack_h2(k1x * e0.x - k2x * e0.y, k1y * e1.x - k2y * e1.y);
-    yb[j] = pack_h2(k1x * e0.y + k2x * e0.x, k1y * e1.y + k2y * e1.x);
+  for (int c = 0; c < 4; ++c) {
+    // (k_m, k_{m+32}) -> (k_m cos - k_{m+32} sin, k_m sin + k_{m+32} cos), m = 8u + 2c (+1)
+    const float k1x = bf_lo(xa[c]), k1y = bf_hi(xa[c]), k2x = bf_lo(xb[c]), k2y = bf_hi(xb[c]);
+    const float2 e0 = e[2 * c], e1 = e[2 * c + 1];
+    ya[c] = pack_h2(k1x * e0.x - k2x * e0.y, k1y * e1.x - k2y * e1.y);
+    yb[c] = pack_h2(k1x * e0.y + k2x * e0.x, k1y * e1.y + k2y * e1.x);
   }
   const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
   uint32_t za[4], zb[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    za[j] = pack_h2(bf_lo(wa[j]), bf_hi(wa[j]));
-    zb[j] = pack_h2(bf_lo(wb[j]), bf_hi(wb[j]));
+  for (int c = 0; c < 4; ++c) {
+    za[c] = pack_h2(bf_lo(wa[c]), bf_hi(wa[c]));
+    zb[c] = pack_h2(bf_lo(wb[c]), bf_hi(wb[c]));
   }
-  const int s = swz(p);
+  const int sw = swz(p);
   uint4* ko = reinterpret_cast<uint4*>(kp + row * kD);
   uint4* vo = reinterpret_cast<uint4*>(vp + row * kD);
-  ko[u ^ s] = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-  ko[(u + 4) ^ s] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
-  vo[u ^ s] = make_uint4(za[0], za[1], za[2], za[3]);
-  vo[(u + 4) ^ s] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
+  ko[u ^ sw] = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+  ko[(u + 4) ^ sw] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+  vo[u ^ sw] = make_uint4(za[0], za[1], za[2], za[3]);
+  vo[(u + 4) ^ sw] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
 }
 
 // ------------------------------------------------------------------ attention kernel
 template <int MODE>
-__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 4 : 3) fwd_tc_kernel(TcArgs a) {
+__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : 3) fwd_tc_kernel(TcArgs a) {
   __shared__ KeySmem ks;
   __shared__ __align__(8) uint64_t full_bar[kSlots];
   __shared__ __align__(8) uint64_t empty_bar[kSlots];
@@ -507,7 +518,10 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? 4 : 3) fwd_tc_kernel(T
       }
       act[cc] = __any_sync(0xffffffffu, ok[0][cc] || ok[1][cc]);
     }
-    if (act[0] || act[1]) {  // uniform; the chunk's MMAs in one block, free to overlap
+    bool any_act = false;
+#pragma unroll
+    for (int cc = 0; cc < kRungChunk; ++cc) any_act |= act[cc];
+    if (any_act) {  // uniform; the chunk's MMAs in one block, free to overlap
       float C[kRungChunk][2][4];
 #pragma unroll
       for (int cc = 0; cc < kRungChunk; ++cc) {
@@ -644,19 +658,23 @@ size_t fwd_tc_workspace_bytes(int B, int H, int N) {
   return static_cast<size_t>(B) * H * N * kD * 2 * sizeof(__half);
 }
 
-cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k,
-                          const void* v, void* o, float* lse, const float2* lo_tab,
-                          const float2* hi_tab, int* status, unsigned long long wait_ns,
-                          int skip_first_rung_copy, void* workspace, cudaStream_t stream) {
+cudaError_t launch_prep_kv(int B, int H, int N, const void* k, const void* v, const float2* lo_tab,
+                           const float2* hi_tab, void* workspace, cudaStream_t stream) {
   const long long rows = static_cast<long long>(B) * H * N;
   __half* kp = static_cast<__half*>(workspace);
   __half* vp = kp + rows * kD;
-  const long long prep_blocks = (rows * 4 + 255) / 256;
-  if (prep_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  prep_kv_kernel<<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
+  const long long blocks = (rows * 4 + 255) / 256;  // four threads a row
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  prep_kv_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), kp, vp, lo_tab, hi_tab, N,
       rows);
+  return cudaGetLastError();
+}
 
+cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* workspace,
+                          void* o, float* lse, const float2* lo_tab, const float2* hi_tab, int* status,
+                          unsigned long long wait_ns, int skip_first_rung_copy, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(B) * H * N;
   TcArgs a;
   a.t = t;
   a.N = N;
@@ -665,8 +683,8 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   a.slab_rows = t.mode == 1 ? kTcTile + 8 : kTcTile;
   a.slot_bytes = 2 * a.slab_rows * kRowBytes;
   a.q = static_cast<const __nv_bfloat16*>(q);
-  a.kp = kp;
-  a.vp = vp;
+  a.kp = static_cast<const __half*>(workspace);
+  a.vp = a.kp + rows * kD;
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
   a.rope_lo = lo_tab;

@@ -26,7 +26,8 @@ FIB_HEAD_DIM, FIB_MAX_RUNGS, FIB_MAX_WINDOW, FIB_MAX_LAYERS = 64, 32, 64, 256
 EXPORTS = [
     "fib_attn_error_string", "fib_attn_base", "fib_attn_schedule", "fib_attn_mask_distances",
     "fib_attn_interp_rungs", "fib_attn_plan_create", "fib_attn_plan_destroy",
-    "fib_attn_plan_distances", "fib_attn_fwd_workspace_size", "fib_attn_fwd", "fib_attn_bwd_workspace_size", "fib_attn_bwd",
+    "fib_attn_plan_distances", "fib_attn_fwd_workspace_size", "fib_attn_fwd",
+    "fib_attn_fwd_prepare_kv", "fib_attn_fwd_attend", "fib_attn_bwd_workspace_size", "fib_attn_bwd",
     "fib_attn_debug_indices", "fib_attn_last_device_status", "fib_attn_plan_set_debug",
     "fib_attn_bwd_noalloc", "fib_attn_decode",
 ]
@@ -49,6 +50,8 @@ _SIGS = {
     "fib_attn_plan_destroy": (_i, [_vp]),
     "fib_attn_plan_distances": (_i, [_vp, _i, _i, _i32p, _i, ctypes.POINTER(_i)]),
     "fib_attn_fwd_workspace_size": (ctypes.c_size_t, [_vp, _i, _i, _i, _i]),
+    "fib_attn_fwd_prepare_kv": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "fib_attn_fwd_attend": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]),
     "fib_attn_fwd": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                           _vp]),
     "fib_attn_bwd_workspace_size": (ctypes.c_size_t, [_vp, _i, _i, _i]),
@@ -223,6 +226,36 @@ def fib_attn_fwd(plan: Plan, layer: int, q, k, v, o=None, lse=None, alpha_dev=No
     _check("fib_attn_fwd", lib().fib_attn_fwd(
         plan.handle, layer, B, H, N, _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
         _ptr(alpha_dev), _ptr(workspace), ws_bytes, _stream(stream)))
+    return o, lse
+
+
+def fib_attn_fwd_prepare_kv(plan: Plan, k, v, workspace=None, stream=None):
+    """K rotated at its own positions and V, as float16, into a workspace (allocated by torch
+    when not given), for fib_attn_fwd_attend; returns the workspace."""
+    B, H, N = _shape(k)
+    _same(k, v)
+    need = fib_attn_fwd_workspace_size(plan, B, H, N, k.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=k.device)
+    _check("fib_attn_fwd_prepare_kv", lib().fib_attn_fwd_prepare_kv(
+        plan.handle, B, H, N, _DT[k.dtype], _ptr(k), _ptr(v), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return workspace
+
+
+def fib_attn_fwd_attend(plan: Plan, layer: int, q, workspace, o=None, lse=None, alpha_dev=None,
+                        want_lse: bool = True, stream=None):
+    """Attention of q against a workspace filled by fib_attn_fwd_prepare_kv; returns (o, lse)."""
+    B, H, N = _shape(q)
+    _same(q, o)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check("fib_attn_fwd_attend", lib().fib_attn_fwd_attend(
+        plan.handle, layer, B, H, N, _DT[q.dtype], _ptr(q), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(o), _ptr(lse), _ptr(alpha_dev),
+        _stream(stream)))
     return o, lse
 
 

@@ -141,6 +141,22 @@ int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
                  const void* q, const void* k, const void* v, void* o, float* lse,
                  const float* alpha_dev, void* workspace, size_t ws_bytes, void* stream);
 
+/* The two halves of the bf16 forward, for callers that reuse the prepared keys and values
+ * (several query sets against one K/V) or time the halves apart.  fib_attn_fwd(...) ==
+ * fib_attn_fwd_prepare_kv then fib_attn_fwd_attend on the same stream, bit for bit.
+ * prepare_kv writes into workspace (sized by fib_attn_fwd_workspace_size) K rotated at each
+ * row's own position (the RoPE of "Attended set": keys rotated before they are gathered)
+ * and V, both as float16 [B, H, N, 64]; its layout inside the workspace is private to the
+ * library.  attend reads q and a workspace that prepare_kv filled for the same plan, B, H
+ * and N (not checked) and writes o and lse as fib_attn_fwd.  Both return
+ * FIB_ERR_UNSUPPORTED where the workspace size is 0 (float32, or W > 16), else the
+ * errors of fib_attn_fwd.                                                              */
+int fib_attn_fwd_prepare_kv(fib_attn_plan_t p, int B, int H, int N, int dtype, const void* k,
+                            const void* v, void* workspace, size_t ws_bytes, void* stream);
+int fib_attn_fwd_attend(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
+                        const void* q, const void* workspace, size_t ws_bytes, void* o,
+                        float* lse, const float* alpha_dev, void* stream);
+
 /* ------------------------------------------------------------------------ decode ----
  * One new token per (b, h) against a KV cache (Key results 2, "Efficiency": inference
  * latency of the mask and the interpolated path).  The token sits at position pos of a

@@ -6,9 +6,9 @@ Tolerances:
     against the oracle run on the same bf16-rounded values, plus the bf16 output's own
     rounding (at most half an ulp, bounded by 2^-8 |O|);
   * LSE (float32 output): 1e-5 (float32 inputs); 5e-3 for bf16 inputs: the tensor-core
-    window rounds the RoPE-rotated Q' and K' to f16 (11-bit significand), so a 64-term
-    score carries up to ~1e-3 of rounding error, which LSE inherits (the O bound above
-    is the binding one);
+    path rounds the RoPE-rotated Q' and K' to f16 (11-bit significand) for the window and
+    every rung, so a 64-term score carries up to ~1e-3 of rounding error, which LSE
+    inherits (the O bound above is the binding one);
   * dQ, dK, dV, dalpha: relative L2 <= 2e-2.
 """
 import json
@@ -336,6 +336,36 @@ def test_edge_cases_bf16(mode, N, W, alpha, kind):
     _check_o(o, O_ref, "bf16", f"edge N={N} W={W} {mode}")
     _check_lse(lse, lse_ref, "bf16")
     assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    plan.close()
+
+
+# ------------------------------------------------------------------ prepared halves
+@pytest.mark.parametrize("mode", ["mask", "interp"])
+def test_prepare_then_attend_equals_the_fused_call(mode):
+    """fib_attn_fwd == fib_attn_fwd_prepare_kv + fib_attn_fwd_attend bit for bit, and one
+    prepared K/V serves a second query set."""
+    B, H, N, W = 2, 2, 1000, 12
+    plan = _plan("fib", [0.8, 1.3], W, N, mode)
+    q, k, v = (t.cuda() for t in inputs.qkv(B, H, N, 64, 7, 0, "bf16"))
+    q2 = inputs.qkv(B, H, N, 64, 7, 1, "bf16")[0].cuda()
+    o1, l1 = fa.fib_attn_fwd(plan, 1, q, k, v)
+    ws = fa.fib_attn_fwd_prepare_kv(plan, k, v)
+    assert ws.numel() == fa.fib_attn_fwd_workspace_size(plan, B, H, N, torch.bfloat16)
+    o2, l2 = fa.fib_attn_fwd_attend(plan, 1, q, ws)
+    o3, l3 = fa.fib_attn_fwd_attend(plan, 1, q2, ws)
+    o4, l4 = fa.fib_attn_fwd(plan, 1, q2, k, v)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(o3, o4) and torch.equal(l3, l4)
+    # float32 has no prepared path
+    lib = fa.lib()
+    qf = q.float()
+    s = torch.cuda.current_stream().cuda_stream
+    assert lib.fib_attn_fwd_prepare_kv(plan.handle, B, H, N, fa.FIB_DTYPE_F32, qf.data_ptr(), qf.data_ptr(),
+                                       ws.data_ptr(), ws.numel(), s) == fa.FIB_ERR_UNSUPPORTED
+    assert lib.fib_attn_fwd_attend(plan.handle, 1, B, H, N, fa.FIB_DTYPE_BF16, q.data_ptr(), ws.data_ptr(),
+                                   ws.numel() - 1, o2.data_ptr(), None, None, s) == fa.FIB_ERR_INVALID_ARG
+    assert lib.fib_attn_fwd_attend(plan.handle, 1, B, H, N, fa.FIB_DTYPE_BF16, q.data_ptr(), q.data_ptr(),
+                                   ws.numel(), o2.data_ptr(), None, None, s) == fa.FIB_ERR_INVALID_ARG
     plan.close()
 
 
