@@ -102,23 +102,33 @@ def ncu_traffic(workload):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle sampling during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock/throttle sampling, every 20 ms, started before the warm-up (the tool
+    takes a while to start); summary() keeps the samples stamped inside the timed region
+    marked by mark_start()/mark_end()."""
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index):
         self.dev = device_index
         self.proc = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)  # let the first samples arrive before the timed region
         except Exception:
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *a):
         self.lines = []
@@ -132,24 +142,31 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
-        sm, smax, reasons = [], None, set()
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for l in getattr(self, "lines", []):
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax = float(f[2])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[1]), float(f[2]),
+                             {n for n, v in zip(names, f[5:9]) if v.lower().startswith("active")}))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.02 <= r[0] <= self.t1 + 0.02]
+        # a timed region shorter than the sampling period may hold no sample: then the two
+        # samples around it stand for it
+        use = inside
+        if not use and self.t0 is not None:
+            mid = (self.t0 + self.t1) / 2
+            use = sorted(rows, key=lambda r: abs(r[0] - mid))[:2]
+        if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = set().union(*(r[3] for r in use))
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": use[-1][2],
+                "reasons": sorted(reasons), "samples": len(use), "samples_inside_timed_region": len(inside)}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -236,19 +253,21 @@ def time_device(w, steps, warmup, device, rank, world):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         run_stack(fa, plan, dev, outs, lses, adev, wss)
-    for _ in range(warmup):
-        graph.replay()
-    torch.cuda.synchronize(device)
-    if world > 1:
-        torch.distributed.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(device.index if device.index is not None else 0) as clk:
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize(device)
+        if world > 1:
+            torch.distributed.barrier()
+        clk.mark_start()
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(steps):
                 graph.replay()
             e1.record(stream)
         torch.cuda.synchronize(device)
+        clk.mark_end()
     ms = e0.elapsed_time(e1)
     if world > 1:
         t = torch.tensor([ms], device=device)
@@ -344,7 +363,7 @@ def oracle_tokens_per_s(w, per_layer_s):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
