@@ -43,7 +43,10 @@
 
 namespace fibattn {
 
-constexpr int kTcWarps = 4;                    // compute warps (16 queries each)
+#ifndef FIB_TC_WARPS
+#define FIB_TC_WARPS 4
+#endif
+constexpr int kTcWarps = FIB_TC_WARPS;         // compute warps (16 queries each)
 constexpr int kTcTile = 16 * kTcWarps;         // queries per CTA
 constexpr int kConsumers = 32 * kTcWarps;
 constexpr int kTcThreads = kConsumers + 32;    // + one producer warp
@@ -56,6 +59,9 @@ constexpr int kTcMaxW = 16;
 #endif
 #ifndef FIB_TC_MIN_CTAS
 #define FIB_TC_MIN_CTAS 4
+#endif
+#ifndef FIB_TC_MIN_CTAS_INTERP
+#define FIB_TC_MIN_CTAS_INTERP 3
 #endif
 constexpr int kSlots = FIB_TC_SLOTS;           // ring slots
 constexpr int kRungChunk = FIB_TC_CHUNK;       // rungs per online-softmax step
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const __nv_bfloat16* __res
 
 // ------------------------------------------------------------------ attention kernel
 template <int MODE>
-__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : 3) fwd_tc_kernel(TcArgs a) {
+__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_TC_MIN_CTAS_INTERP) fwd_tc_kernel(TcArgs a) {
   __shared__ KeySmem ks;
   __shared__ __align__(8) uint64_t full_bar[kSlots];
   __shared__ __align__(8) uint64_t empty_bar[kSlots];
