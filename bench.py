@@ -43,7 +43,9 @@ WORKLOADS = {
                                 mode="interp", dtype="bf16", cfg=4),
 }
 DEFAULT = "linear-stack-n1024"
-SECONDARY = ["coprime-fib-n4096", "coprime-pow2-n4096"]
+SECONDARY = ["coprime-fib-n4096", "coprime-pow2-n4096", "learned-interp-n1024", "long-mask-n131072",
+             "long-interp-n131072"]
+BACKWARD = "learned-interp-n1024"  # the training configuration: interpolated path, learned alpha
 
 
 def alphas_for(w):
@@ -62,6 +64,12 @@ def alphas_for(w):
 def compulsory_bytes(w):
     elt = 2 if w["dtype"] == "bf16" else 4
     return w["B"] * w["H"] * w["N"] * 64 * elt * 4  # Q, K, V read once + O written once
+
+
+def compulsory_bytes_bwd(w):
+    elt = 2 if w["dtype"] == "bf16" else 4
+    # Q, K, V, O, dO read once + dQ, dK, dV written once (LSE and Delta apart)
+    return w["B"] * w["H"] * w["N"] * 64 * elt * 8
 
 
 def read_peaks():
@@ -311,6 +319,36 @@ def time_device(w, steps, warmup, device, rank, world):
     return res
 
 
+def time_backward(w, steps, warmup, device):
+    """Backward of the L-layer stack (dQ, dK, dV and dalpha of every layer), replayed from a
+    CUDA graph: milliseconds per step and per launch of the backward."""
+    import torch
+    from fibonacci_offset_sparse_gb300 import fib_attn as fa
+    from fibonacci_offset_sparse_gb300 import inputs
+    plan, host, dev, outs, lses, adev, wss = setup(w, device)
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        run_stack(fa, plan, dev, outs, lses, adev, wss)
+    dOs = [inputs.upstream_grad(w["B"], w["H"], w["N"], 64, w["cfg"], l, w["dtype"]).to(device)
+           for l in range(w["L"])]
+    grads = [tuple(torch.empty_like(d[0]) for _ in range(3)) for d in dev]
+    dal = [torch.empty(1, dtype=torch.float32, device=device) for _ in dev]
+    need = fa.fib_attn_bwd_workspace_size(plan, w["B"], w["H"], w["N"])
+    bws = [torch.empty(need, dtype=torch.uint8, device=device) for _ in dev]
+
+    def bwd_stack():
+        for l, (q, k, v) in enumerate(dev):
+            fa.fib_attn_bwd(plan, l, q, k, v, outs[l], lses[l], dOs[l], *grads[l], dalpha=dal[l],
+                            alpha_dev=adev, workspace=bws[l])
+
+    with torch.cuda.stream(stream):
+        bwd_stack()
+    torch.cuda.synchronize(device)
+    ms = time_graph(torch, stream, device, bwd_stack, steps, warmup)
+    plan.close()
+    return {"ms_per_step": ms, "us_per_layer": ms * 1e3 / w["L"]}
+
+
 def time_dense_sdpa(w, device, reps=20):
     """Dense causal attention on the same shape through PyTorch's fused attention (a library
     kernel, timed only as the dense comparison point): milliseconds per layer."""
@@ -458,12 +496,22 @@ def main():
             la = rs["halves"]["attend_ms"] / 1e3 if rs["halves"] else ls
             ach = compulsory_bytes(ws) / la / 1e9
             sec[name] = {"value": ws["B"] * ws["N"] * world / (rs["ms_per_step"] / 1e3), "unit": UNIT,
+                         "path": ws["mode"] + " forward", "layers": ws["L"],
                          "ms_per_step": rs["ms_per_step"], "us_per_layer": ls * 1e6,
                          "attend_us_per_launch": la * 1e6,
                          "prepare_us_per_launch": rs["halves"]["prepare_ms"] * 1e3 if rs["halves"] else None,
                          "achieved_gbs": ach, "frac": ach / peak,
                          "layer_frac": compulsory_bytes(ws) / ls / 1e9 / peak, "traffic": ncu_traffic(name)}
         line["secondary"] = sec
+        wb = WORKLOADS[BACKWARD]
+        rb = time_backward(wb, args.steps, args.warmup, device)
+        bb = compulsory_bytes_bwd(wb)
+        line["backward"] = {"workload": BACKWARD, "path": "interp backward (dQ, dK, dV, dalpha)",
+                            "value": wb["B"] * wb["N"] * world / (rb["ms_per_step"] / 1e3), "unit": UNIT,
+                            "ms_per_step": rb["ms_per_step"], "us_per_layer": rb["us_per_layer"],
+                            "compulsory_bytes_per_layer": bb,
+                            "achieved_gbs": bb / (rb["us_per_layer"] * 1e-6) / 1e9,
+                            "frac": bb / (rb["us_per_layer"] * 1e-6) / 1e9 / peak}
     try:
         dense = {}
         for name in [args.workload] + (SECONDARY if args.workload == DEFAULT and not args.no_secondary else []):
