@@ -84,7 +84,7 @@ def read_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for fn in ("common.cuh", "fwd.cu", "fwd_tc.cu"):
+    for fn in ("common.cuh", "tc_common.cuh", "fwd.cu", "fwd_tc.cu"):
         with open(os.path.join(ROOT, "fibonacci_offset_sparse_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -29,6 +29,12 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
 cudaError_t launch_debug_indices(const LayerTable& t, int N, int i0, int i1, int32_t* out,
                                  float* w_out, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int H, int N);
+bool bwd_tc_supported(const LayerTable& t);
+size_t bwd_tc_workspace_bytes(int B, int H, int N);
+cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k, const void* v,
+                          const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                          float* dalpha, void* ws, const float2* lo_tab, const float2* hi_tab, int* status,
+                          unsigned long long wait_ns, cudaStream_t stream);
 cudaError_t launch_bwd(const LayerTable& t, int B, int H, int N, int dtype, const void* q,
                        const void* k, const void* v, const void* o, const float* lse,
                        const void* dO, void* dq, void* dk, void* dv, float* dalpha, void* ws,
@@ -387,6 +393,8 @@ int fib_attn_decode(fib_attn_plan_t p, int layer, int B, int H, int N, int pos, 
 
 size_t fib_attn_bwd_workspace_size(fib_attn_plan_t p, int B, int H, int N) {
   if (p == nullptr || B < 1 || H < 1 || N < 1) return 0;
+  // one size for both dtypes: the bf16 tensor-core path (W <= 16) needs the prepared rows
+  if (p->W <= 16) return std::max(bwd_workspace_bytes(B, H, N), bwd_tc_workspace_bytes(B, H, N));
   return bwd_workspace_bytes(B, H, N);
 }
 
@@ -401,7 +409,7 @@ int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, c
     return FIB_ERR_INVALID_ARG;
   if (lse == nullptr || !aligned(lse, 4) || dalpha == nullptr || !aligned(dalpha, 4)) return FIB_ERR_INVALID_ARG;
   if (alpha_dev != nullptr && !aligned(alpha_dev, 4)) return FIB_ERR_INVALID_ARG;
-  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < bwd_workspace_bytes(B, H, N))
+  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < fib_attn_bwd_workspace_size(p, B, H, N))
     return FIB_ERR_INVALID_ARG;
   const void* ins[] = {q, k, v, o, dO};
   const void* outs[] = {dq, dk, dv};
@@ -414,6 +422,11 @@ int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, c
   LayerTable t;
   st = make_table(p, layer, N, p->mode == FIB_MODE_INTERP ? alpha_dev : nullptr, &t);
   if (st != FIB_OK) return st;
+  // bf16 with a window of at most 16 keys: prepared rows + tensor-core kernels (bwd_tc.cu);
+  // otherwise the CUDA-core kernels (bwd.cu), which also serve float32
+  if (dtype == FIB_DTYPE_BF16 && bwd_tc_supported(t))
+    return cuda_status(launch_bwd_tc(t, B, H, N, q, k, v, o, lse, dO, dq, dk, dv, dalpha, workspace, p->d_lo,
+                                     p->d_hi, p->d_status, p->wait_ns, static_cast<cudaStream_t>(stream)));
   return cuda_status(launch_bwd(t, B, H, N, dtype, q, k, v, o, lse, dO, dq, dk, dv, dalpha,
                                 workspace, p->d_lo, p->d_hi, static_cast<cudaStream_t>(stream)));
 }

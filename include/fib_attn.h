@@ -176,7 +176,10 @@ int fib_attn_decode(fib_attn_plan_t p, int layer, int B, int H, int N, int pos, 
  * dalpha: device float32 scalar, written (not accumulated) with dl/dalpha_layer in
  * INTERP mode and 0 in MASK mode (static distances carry no alpha gradient).
  * workspace: device scratch of at least fib_attn_bwd_workspace_size(p, B, H, N) bytes,
- * 256-byte aligned, caller-owned; its contents on entry are ignored.
+ * 256-byte aligned, caller-owned; its contents on entry are ignored.  The size is the same
+ * for both dtypes: for a plan with W <= 16 it is what the bf16 path needs (Q, K, V, dO
+ * prepared once as float16 rows, B*H*N*512 bytes, plus Delta and the dalpha partials);
+ * the float32 path uses only the first B*H*N*4 bytes and the partials.
  * Errors as fib_attn_fwd, plus FIB_ERR_INVALID_ARG for a short/misaligned workspace.  */
 size_t fib_attn_bwd_workspace_size(fib_attn_plan_t p, int B, int H, int N);
 int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
@@ -189,10 +192,12 @@ int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
  * callers that cannot allocate device memory on the call path -- for example a plugin inside
  * a framework that owns the device heap, or a real-time loop that forbids allocation -- and
  * so cannot hand fib_attn_bwd a workspace.  Same arguments, results and errors as
- * fib_attn_bwd without workspace/ws_bytes: the scratch is a fixed 8 MiB device array inside
- * the library, held on every device that loads it until the process exits.  A call needing
- * more (fib_attn_bwd_workspace_size(p, B, H, N) > 8 MiB, i.e. B*H*N above about two
- * million) returns FIB_ERR_INVALID_ARG before any launch.  The first call on a device looks
+ * fib_attn_bwd without workspace/ws_bytes (for bf16 within fib_attn_bwd's bound, not bit for
+ * bit: this entry point always runs the CUDA-core kernels, which need no prepared rows): the
+ * scratch is a fixed 8 MiB device array inside the library, held on every device that
+ * loads it until the process exits.  A call whose CUDA-core scratch (4 bytes per
+ * query-head plus 4 per 64-query tile) exceeds 8 MiB, i.e. B*H*N above about two million,
+ * returns FIB_ERR_INVALID_ARG before any launch.  The first call on a device looks
  * up the array's device address and caches it (host-side work; make that first call before
  * any stream capture).  Every call shares the array and it keeps the last call's contents
  * (nothing in it needs zeroing); calls whose kernels overlap on the GPU race on it.  Nothing

@@ -263,6 +263,47 @@ def test_backward_fp32(mode, alpha, device_alpha):
     plan.close()
 
 
+@pytest.mark.parametrize("mode,alpha,W,N", [("mask", 0.5 + 4 / 15, 12, 1000), ("mask", 1.5, 16, 333),
+                                             ("mask", 1.0, 1, 200), ("interp", 1.2345, 8, 1000),
+                                             ("interp", 0.6789, 16, 333), ("interp", 1.0, 10, 517),
+                                             ("interp", 1.5, 1, 130)])
+@pytest.mark.parametrize("device_alpha", [False, True])
+def test_backward_bf16_tensor_core(mode, alpha, W, N, device_alpha):
+    """The bf16 backward (tensor-core path for W <= 16) against the oracle's gradients of its
+    own forward: relative L2 of dQ, dK, dV and dalpha; ragged N (not a multiple of the 64-row
+    tiles), windows 1..16, alpha = 1.0 (every interp weight 0: the partner-row term of
+    dalpha), and a second run that must give identical bits."""
+    B, H = 2, 2
+    if device_alpha:
+        alpha = float(np.float32(alpha))
+    plan = _plan("fib", [alpha], W, N, mode)
+    q, k, v = inputs.qkv(B, H, N, 64, 210, 0, "bf16")
+    dO = inputs.upstream_grad(B, H, N, 64, 210, 0, "bf16")
+    adev = torch.tensor([alpha], dtype=torch.float32, device="cuda") if device_alpha else None
+    qc, kc, vc, dOc = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+    o, lse = fa.fib_attn_fwd(plan, 0, qc, kc, vc, alpha_dev=adev)
+    dq, dk, dv, da = fa.fib_attn_bwd(plan, 0, qc, kc, vc, o, lse, dOc, alpha_dev=adev)
+    torch.cuda.synchronize()
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    qf, kf, vf, gf = (inputs.as_f64(x) for x in (q, k, v, dO))
+    rq, rk, rv, ra = oracle.attend_bwd(qf, kf, vf, gf, alpha, oracle.fibonacci_base(), W, mode)
+    what = f"{mode} alpha={alpha} W={W} N={N}"
+    for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        e = _rel_l2(g.double().cpu().numpy(), r)
+        _record("bwd_rel_l2_" + name, what, e)
+        assert e <= REL_L2, f"{what} {name} rel-L2 {e:.3e}"
+    if mode == "mask":
+        assert float(da.item()) == 0.0
+    else:
+        e = abs(float(da.item()) - ra) / max(abs(ra), 1e-30)
+        _record("bwd_rel_dalpha", what, e)
+        assert e <= REL_L2, f"{what} dalpha {da.item()} vs {ra} rel {e:.3e}"
+    dq2, dk2, dv2, da2 = fa.fib_attn_bwd(plan, 0, qc, kc, vc, o, lse, dOc, alpha_dev=adev)
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2) and torch.equal(da, da2)
+    plan.close()
+
+
 # ------------------------------------------------------------------ error paths on a GPU
 def test_device_error_paths():
     plan = _plan("fib", [1.0, 1.0], 12, 256, "mask")

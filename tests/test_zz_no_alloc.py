@@ -39,7 +39,10 @@ def test_noalloc_backward_matches_workspace_backward_twice(dtype, mode, alpha):
     B, H, N, W = 2, 3, 333, 8
     m = fa.FIB_MODE_MASK if mode == "mask" else fa.FIB_MODE_INTERP
     plan = fa.fib_attn_plan_create(fa.FIB_BASE_FIBONACCI, [alpha, alpha], W, N, m)
-    # the tolerances of the other backward tests: fp32 rel-L2 1e-5, bf16 rel-L2 2e-2
+    # the tolerances of the other backward tests: fp32 rel-L2 1e-5, bf16 rel-L2 2e-2.  For
+    # bf16 the two entry points run different kernels (the ordinary one the tensor-core path
+    # with its prepared float16 rows, the allocation-free one the CUDA-core path, which needs
+    # no such scratch), so they agree to the bf16 bound, not bit for bit.
     tol = 1e-5 if dtype == "f32" else 2e-2
     for call in range(2):  # two calls in a row: the second starts from the first one's scratch
         q, k, v = (t.cuda() for t in inputs.qkv(B, H, N, 64, 700 + call, call, dtype))
@@ -59,7 +62,8 @@ def test_noalloc_backward_matches_workspace_backward_twice(dtype, mode, alpha):
         if mode == "mask":
             assert float(da.item()) == 0.0 == float(ra.item())
         else:
-            assert abs(float(da.item()) - float(ra.item())) <= 1e-4 * abs(float(ra.item())) + 1e-4
+            rel = 1e-4 if dtype == "f32" else 2e-2
+            assert abs(float(da.item()) - float(ra.item())) <= rel * abs(float(ra.item())) + 1e-4
     plan.close()
 
 
