@@ -22,6 +22,7 @@
 //     dP^T = V'.dO'^T, then dk' += dS^T Q's and dv += P^T dO'.
 // Precision as the forward: f16 operands (Q's, K', V', dO', P, dS), f32 accumulation.
 #include <algorithm>
+#include <type_traits>
 
 #include "tc_common.cuh"
 
@@ -411,7 +412,7 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
       // dq' += diag(dS (1-w)) K'[slab rows] (+ diag(dS w) K'[rows - 1])
 #pragma unroll
       for (int part = 0; part < (MODE == 1 ? 2 : 1); ++part) {
-        if (part == 1 && !(w > 0.f)) break;  // uniform
+        if (part == 1 && !(w > 0.f)) continue;  // uniform
         const float f = MODE == 1 ? (part == 0 ? 1.f - w : w) : 1.f;
         const float x0 = ds[0] * f, x1 = ds[1] * f;
         const uint32_t a0 = pack_h2(x0 * sel_lo, x0 * sel_hi);
@@ -669,43 +670,41 @@ __global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
       }
     wait_stage(n);
     const unsigned char* qst = slot_of(n);
-#pragma unroll
-    for (int role = 0; role < (MODE == 1 ? 2 : 1); ++role) {
-      if (role == 1 && !(w > 0.f)) break;  // uniform: weight 0
+    // role as a compile-time constant, so that nothing below is indexed at run time
+    auto do_role = [&](auto role_c) {
+      constexpr int role = decltype(role_c)::value;
       bool ok[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h)
         ok[h] = !s_err && k0 + g + 8 * h <= j_last && qi[role][h] < N && qi[role][h] >= ks.need[c];
-      if (!__any_sync(0xffffffffu, ok[0] || ok[1])) continue;  // uniform
-      // B fragments: column g of n-tile h = query of key k0 + g + 8h, slab row x
-      uint32_t bq[2][2][4], bg[2][2][4];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int x = min(16 * warp + g + 8 * h + role, xlast);
-        lds_kfrag(reinterpret_cast<const uint4*>(qst + x * kRowBytes), t, qfirst + x, bq[h][0], bq[h][1]);
-        lds_kfrag(reinterpret_cast<const uint4*>(qst + kQ2 + x * kRowBytes), t, qfirst + x, bg[h][0], bg[h][1]);
-      }
-      // scores and dP against the query's rows r0 = j + role and (interp) r1 = j + role - 1
+      if (!__any_sync(0xffffffffu, ok[0] || ok[1])) return;  // uniform
+      // scores and dP against the query's rows r0 = j + role and (interp) r1 = j + role - 1;
+      // B fragments: column g of n-tile h = query of key k0 + g + 8h (slab row x)
       float sc[2][2], dp[2][2];  // [row part][h]
 #pragma unroll
       for (int part = 0; part < (MODE == 1 ? 2 : 1); ++part) {
         const int off = role - part;
-        uint32_t ak[2][2][4], av[2][2][4];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int p = k0 + g + 8 * h + off;
-          lds_kfrag(own_row(0, p), t, own_pos(p), ak[h][0], ak[h][1]);
-          lds_kfrag(own_row(1, p), t, own_pos(p), av[h][0], av[h][1]);
-        }
+        // S against K' rows, then dP against V' rows: one operand set live at a time
         float C[2][4], E[2][4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int kv = 0; kv < 2; ++kv) {
+          uint32_t aa[2][2][4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) C[h][u] = E[h][u] = 0.f;
+          for (int h = 0; h < 2; ++h) {
+            const int p = k0 + g + 8 * h + off;
+            lds_kfrag(own_row(kv, p), t, own_pos(p), aa[h][0], aa[h][1]);
+          }
 #pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            mma16816(C[h], ak[0][0][s], ak[1][0][s], ak[0][1][s], ak[1][1][s], bq[h][0][s], bq[h][1][s]);
-            mma16816(E[h], av[0][0][s], av[1][0][s], av[0][1][s], av[1][1][s], bg[h][0][s], bg[h][1][s]);
+          for (int h = 0; h < 2; ++h) {
+            const int x = min(16 * warp + g + 8 * h + role, xlast);
+            uint32_t bl[4], bh2[4];
+            lds_kfrag(reinterpret_cast<const uint4*>(qst + kv * kQ2 + x * kRowBytes), t, qfirst + x, bl, bh2);
+            float (&acc)[4] = kv == 0 ? C[h] : E[h];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc[u] = 0.f;
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              mma16816(acc, aa[0][0][s], aa[1][0][s], aa[0][1][s], aa[1][1][s], bl[s], bh2[s]);
           }
         }
         sc[part][0] = __shfl_sync(0xffffffffu, (g & 1) ? C[0][1] : C[0][0], src_lane);
@@ -717,9 +716,9 @@ __global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
       float xs[2], xp[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const float s = MODE == 1 ? (1.f - w) * sc[0][h] + w * sc[1][h] : sc[0][h];
+        const float sv = MODE == 1 ? (1.f - w) * sc[0][h] + w * sc[1][h] : sc[0][h];
         const float dpp = MODE == 1 ? (1.f - w) * dp[0][h] + w * dp[1][h] : dp[0][h];
-        const float P = ok[h] ? exp2f(s - lq[role][h]) : 0.f;
+        const float P = ok[h] ? exp2f(sv - lq[role][h]) : 0.f;
         xs[h] = wt * P * (dpp - dd[role][h]);
         xp[h] = wt * P;
       }
@@ -739,7 +738,9 @@ __global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
         mma16816(dV[nd], p0, 0u, 0u, p3, c4[0], c4[1]);
         mma16816(dV[nd + 1], p0, 0u, 0u, p3, c4[2], c4[3]);
       }
-    }
+    };
+    do_role(std::integral_constant<int, 0>{});
+    if (MODE == 1 && w > 0.f) do_role(std::integral_constant<int, 1>{});  // uniform: weight w
     release_stage(n);
   }
 
