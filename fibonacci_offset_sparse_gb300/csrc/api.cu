@@ -30,7 +30,7 @@ cudaError_t launch_debug_indices(const LayerTable& t, int N, int i0, int i1, int
                                  float* w_out, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int H, int N);
 bool bwd_tc_supported(const LayerTable& t);
-size_t bwd_tc_workspace_bytes(int B, int H, int N);
+size_t bwd_tc_workspace_bytes(int B, int H, int N, int W);
 cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k, const void* v,
                           const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
                           float* dalpha, void* ws, const float2* lo_tab, const float2* hi_tab, int* status,
@@ -394,7 +394,7 @@ int fib_attn_decode(fib_attn_plan_t p, int layer, int B, int H, int N, int pos, 
 size_t fib_attn_bwd_workspace_size(fib_attn_plan_t p, int B, int H, int N) {
   if (p == nullptr || B < 1 || H < 1 || N < 1) return 0;
   // one size for both dtypes: the bf16 tensor-core path (W <= 16) needs the prepared rows
-  if (p->W <= 16) return std::max(bwd_workspace_bytes(B, H, N), bwd_tc_workspace_bytes(B, H, N));
+  if (p->W <= 16) return std::max(bwd_workspace_bytes(B, H, N), bwd_tc_workspace_bytes(B, H, N, p->W));
   return bwd_workspace_bytes(B, H, N);
 }
 

@@ -14,12 +14,13 @@
 //     with the chunk swizzle of fwd_tc.cu, and Delta (float32), each row read once.
 //   * bwd_q_kernel (query-owned, 64 queries a CTA): the forward's structure, with dP =
 //     dO'.V'^T beside S = Q's.K'^T and dq' += dS K' in place of O += P V'.  Rungs are
-//     diagonals of 16x16 blocks, as in the forward.  Also each CTA's dalpha partial.
-//   * bwd_kv_kernel (key-owned, 64 keys a CTA, no atomics): the rows of the CTA's keys (and
-//     one row either side, the partners of interpolated keys) stay in shared memory; the
-//     queries that read them stream through a ring: the 80-row block [j0, j0+80) for the
-//     window band, then per rung the query slab [j0+lo, j0+lo+65).  S^T = K'.Q's^T and
-//     dP^T = V'.dO'^T, then dk' += dS^T Q's and dv += P^T dO'.
+//     diagonals of 16x16 blocks, as in the forward.  It also writes P and dS of every
+//     attended (query, key slot) -- W + R float pairs a query, the sparse pattern makes
+//     that small -- and each CTA's dalpha partial.
+//   * bwd_kv_kernel (key-owned, 64 keys a CTA, no atomics): a gather, no score is
+//     recomputed.  The queries that read the CTA's keys stream through a ring (the 80-row
+//     block [j0, j0+80) of Q's and dO' for the window band, then per rung the query slab
+//     [j0+lo, j0+lo+65)); with their stored P and dS, dk' += dS^T Q's and dv += P^T dO'.
 // Precision as the forward: f16 operands (Q's, K', V', dO', P, dS), f32 accumulation.
 #include <algorithm>
 #include <type_traits>
@@ -34,7 +35,6 @@ constexpr int kBCons = 32 * kBWarps;
 constexpr int kBThreadsT = kBCons + 32;    // + one producer warp
 constexpr int kBSlots = 3;
 constexpr int kKvQRows = kBTileT + 16;     // query rows a kv stage holds (window block: 80)
-constexpr int kKvOwn = kBTileT + 2;        // own key rows [j0-1, j0+65)
 
 struct BtcArgs {
   LayerTable t;
@@ -53,6 +53,8 @@ struct BtcArgs {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   float* partials;
+  float2* pds;      // (P, dS) of every attended (query, key slot): [B*H*N][pds_stride]
+  int pds_stride;   // W + rungs of the layer table
   const float2* rope_lo;
   const float2* rope_hi;
   int* status;
@@ -327,6 +329,8 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
         const bool ok = dist >= 0 && dist < W && q0 - 16 + c >= 0;
         const float p = ok ? exp2f(S[nt][2 * h + e] - lse2[h]) : 0.f;
         S[nt][2 * h + e] = p * (D[nt][2 * h + e] - dlt[h]);  // dS
+        if (ok && irow[h] < N)  // slot d of query i: the key i - d
+          a.pds[(static_cast<size_t>(bh) * N + irow[h]) * a.pds_stride + dist] = make_float2(p, S[nt][2 * h + e]);
       }
 #pragma unroll
   for (int s2 = 0; s2 < 2; ++s2) {
@@ -402,6 +406,8 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
         const float dpp = MODE == 1 ? (1.f - w) * dp[0][h] + w * dp[1][h] : dp[0][h];
         const float P = ok[h] ? exp2f(s - lse2[h]) : 0.f;
         ds[h] = P * (dpp - dlt[h]);
+        if (ok[h] && t == 0)  // slot W + r of query i (blended P and dS of the rung key)
+          a.pds[(static_cast<size_t>(bh) * N + irow[h]) * a.pds_stride + c] = make_float2(P, ds[h]);
         if (MODE == 1) {
           // dl/dw = dS (s1 - s0) + P (dO.v1 - dO.v0) (natural units), dw/dalpha = f; the
           // partner row i-lo-1 must exist (it only does not when w = 0 and i = lo)
@@ -453,22 +459,20 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
 }
 
 // ------------------------------------------------------------------ key-owned: dk, dv
-// Stage 0 brings the CTA's own K' and V' rows [j0-1, j0+65) (kept for the whole CTA) and
-// the window block's Q's and dO' rows [j0, j0+80); stage 1+r the query slab of rung r:
-// rows [j0+lo, j0+lo+65) of Q's and dO'.
+// Stage 0 brings the window block's Q's and dO' rows [j0, j0+80), stage 1+r the query slab
+// of rung r: rows [j0+lo, j0+lo+65).  P and dS come from bwd_q_kernel.
 template <int MODE>
-__global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
+__global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
   __shared__ KeySmem ks;
   __shared__ __align__(8) uint64_t full_bar[kBSlots];
   __shared__ __align__(8) uint64_t empty_bar[kBSlots];
   __shared__ volatile int s_err;
   extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* own = smem;                                    // K' rows, then V' rows
-  unsigned char* ring = smem + 2 * kKvOwn * kRowBytes;
-  constexpr int kQ2 = kKvQRows * kRowBytes;                     // dO' rows after the Q's rows
+  unsigned char* ring = smem;
+  constexpr int kQ2 = kKvQRows * kRowBytes;  // dO' rows after the Q's rows
 
   const int bh = blockIdx.x % a.bh;
-  const int tile = static_cast<int>(blockIdx.x / a.bh);         // an early key is read by more rungs
+  const int tile = static_cast<int>(blockIdx.x / a.bh);  // an early key is read by more rungs
   const int j0 = tile * kBTileT;
   const int N = a.N;
   const int tid = threadIdx.x;
@@ -511,22 +515,10 @@ __global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
       const int qrows = n == 0 ? kKvQRows : kBTileT + 1;
       const int q1 = min(qfirst + qrows, N);
       const uint32_t qbytes = q1 > qfirst ? static_cast<uint32_t>(q1 - qfirst) * kRowBytes : 0u;
-      uint32_t obytes = 0;
-      int o0 = 0, o1 = 0;
-      if (n == 0) {
-        o0 = max(j0 - 1, 0);
-        o1 = min(j0 + kBTileT + 1, N);
-        obytes = static_cast<uint32_t>(o1 - o0) * kRowBytes;
-      }
-      mbar_arrive_tx(&full_bar[slot], 2 * qbytes + 2 * obytes);
+      mbar_arrive_tx(&full_bar[slot], 2 * qbytes);
       if (qbytes) {
         bulk_g2s(dst, a.qs + base + static_cast<size_t>(qfirst) * kD, qbytes, &full_bar[slot]);
         bulk_g2s(dst + kQ2, a.dos + base + static_cast<size_t>(qfirst) * kD, qbytes, &full_bar[slot]);
-      }
-      if (obytes) {
-        bulk_g2s(own + (o0 - (j0 - 1)) * kRowBytes, a.kp + base + static_cast<size_t>(o0) * kD, obytes, &full_bar[slot]);
-        bulk_g2s(own + (kKvOwn + o0 - (j0 - 1)) * kRowBytes, a.vp + base + static_cast<size_t>(o0) * kD, obytes,
-                 &full_bar[slot]);
       }
       last_n[slot] = n;
     }
@@ -552,15 +544,8 @@ __global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
     if (lane == 0) mbar_arrive(&empty_bar[n % kBSlots]);
   };
   auto slot_of = [&](int n) { return ring + (n % kBSlots) * a.slot_bytes; };
-  // own rows: K' or V' row of position p (j0-1 <= p <= j0+64), clamped to the copied rows
-  const int own_lo = max(j0 - 1, 0), own_hi = min(j0 + kBTileT, N - 1);
-  auto own_row = [&](int kv, int p) {
-    const int pc = min(max(p, own_lo), own_hi);
-    return reinterpret_cast<const uint4*>(own + (kv * kKvOwn + pc - (j0 - 1)) * kRowBytes);
-  };
-  auto own_pos = [&](int p) { return min(max(p, own_lo), own_hi); };
-  const float* lse = a.lse + static_cast<size_t>(bh) * N;
-  const float* dlt = a.delta + static_cast<size_t>(bh) * N;
+  const float2* pds = a.pds + static_cast<size_t>(bh) * N * a.pds_stride;
+  const int stride = a.pds_stride;
 
   float dK[8][4], dV[8][4];  // natural accumulator layout, rows = keys g, g+8
 #pragma unroll
@@ -568,43 +553,10 @@ __global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) dK[nt][c] = dV[nt][c] = 0.f;
 
-  // ---- window band: queries [k0, k0+32) of the warp's 16 keys (query = key + d, d < W)
+  // ---- window band: queries [k0, k0+32) of the warp's 16 keys (query = key + d, d < W).
+  // C-layout element (key row g + 8h, query column c = 8nt + 2t + e): slot d = c - (g + 8h).
   {
-    float lq[4][2], dq[4][2];  // lse2 and Delta of the lane's query columns 8nt + 2t + e
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int i = min(k0 + 8 * nt + 2 * t + e, N - 1);
-        lq[nt][e] = __ldg(lse + i) * kLog2e;
-        dq[nt][e] = __ldg(dlt + i);
-      }
-    wait_stage(0);
-    uint32_t ka[2][2][4], va[2][2][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int p = k0 + g + 8 * h;
-      lds_kfrag(own_row(0, p), t, own_pos(p), ka[h][0], ka[h][1]);
-      lds_kfrag(own_row(1, p), t, own_pos(p), va[h][0], va[h][1]);
-    }
-    const unsigned char* qst = slot_of(0);
-    const int qlast = min(j0 + kKvQRows, N) - 1;  // last copied query row of the block
-    float S[4][4], D[4][4];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) S[nt][c] = D[nt][c] = 0.f;
-      const int qp = min(k0 + 8 * nt + g, qlast);  // column g of n-tile nt (stale beyond: masked)
-      uint32_t bl[4], bh2[4], gl[4], gh[4];
-      lds_kfrag(reinterpret_cast<const uint4*>(qst + (qp - j0) * kRowBytes), t, qp, bl, bh2);
-      lds_kfrag(reinterpret_cast<const uint4*>(qst + kQ2 + (qp - j0) * kRowBytes), t, qp, gl, gh);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        mma16816(S[nt], ka[0][0][s], ka[1][0][s], ka[0][1][s], ka[1][1][s], bl[s], bh2[s]);
-        mma16816(D[nt], va[0][0][s], va[1][0][s], va[0][1][s], va[1][1][s], gl[s], gh[s]);
-      }
-    }
-    // key row kk = g + 8h, query column c = 8nt + 2t + e: d = c - kk
+    float S[4][4], D[4][4];  // dS^T and P^T
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -614,10 +566,13 @@ __global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
           const int c = 8 * nt + 2 * t + e;
           const int d = c - (g + 8 * h);
           const bool ok = d >= 0 && d < W && k0 + c < N && k0 + g + 8 * h < N;
-          const float p = ok ? exp2f(S[nt][2 * h + e] - lq[nt][e]) : 0.f;
-          S[nt][2 * h + e] = p * (D[nt][2 * h + e] - dq[nt][e]);  // dS^T
-          D[nt][2 * h + e] = p;                                   // P^T
+          const float2 v = ok ? __ldg(pds + static_cast<size_t>(k0 + c) * stride + d) : make_float2(0.f, 0.f);
+          D[nt][2 * h + e] = v.x;
+          S[nt][2 * h + e] = v.y;
         }
+    wait_stage(0);
+    const unsigned char* qst = slot_of(0);
+    const int qlast = min(j0 + kKvQRows, N) - 1;  // last copied query row of the block
     // dk' += dS^T Q's, dv += P^T dO' over the 32 queries (k-steps of 16)
 #pragma unroll
     for (int s2 = 0; s2 < 2; ++s2) {
@@ -625,7 +580,7 @@ __global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
       const uint32_t sa2 = pack_h2(S[2 * s2 + 1][0], S[2 * s2 + 1][1]), sa3 = pack_h2(S[2 * s2 + 1][2], S[2 * s2 + 1][3]);
       const uint32_t pa0 = pack_h2(D[2 * s2][0], D[2 * s2][1]), pa1 = pack_h2(D[2 * s2][2], D[2 * s2][3]);
       const uint32_t pa2 = pack_h2(D[2 * s2 + 1][0], D[2 * s2 + 1][1]), pa3 = pack_h2(D[2 * s2 + 1][2], D[2 * s2 + 1][3]);
-      const int qp = min(k0 + 16 * s2 + (mi & 1) * 8 + rl, qlast);
+      const int qp = min(k0 + 16 * s2 + (mi & 1) * 8 + rl, qlast);  // rows past the block: weight 0
       const unsigned char* qrow = qst + (qp - j0) * kRowBytes;
       const int sw = swz(qp);
 #pragma unroll
@@ -643,10 +598,8 @@ __global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
   }
 
   // ---- rungs: key j is read by query i = j + lo + role, as the first (role 0, weight
-  // 1-w) or, interp, the second (role 1, weight w) row of that query's rung key.  Slab row
-  // of query i: i - (j0 + lo).  A query's score needs both of its rows: r0 = i - lo = j + role
-  // and, interp, r1 = r0 - 1, both among the CTA's own rows.
-  const int src_lane = 4 * g + (g >> 1);
+  // 1-w) or, interp, the second (role 1, weight w) row of that query's rung key; slab row
+  // of query i: i - (j0 + lo).  dk' += diag(wt dS) Q's[slab], dv += diag(wt P) dO'[slab].
   const float sel_lo = (t == (g >> 1) && !(g & 1)) ? 1.f : 0.f;
   const float sel_hi = (t == (g >> 1) && (g & 1)) ? 1.f : 0.f;
   for (int r = 0; r < nrk; ++r) {
@@ -654,77 +607,29 @@ __global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
     const int c = W + r;
     const int lo = ks.lo[c];
     const float w = MODE == 1 ? ks.w[c] : 0.f;
+    const int need = ks.need[c];
     const int qfirst = j0 + lo;
     const int xlast = min(qfirst + kBTileT, N - 1) - qfirst;  // last copied slab row
-    // lse2 and Delta of the queries of the lane's two keys, both roles (loads overlap the wait)
-    float lq[2][2], dd[2][2];
-    int qi[2][2];
+    float2 v[2][2];  // [role][h]: stored (P, dS) of the query of key k0 + g + 8h
 #pragma unroll
     for (int role = 0; role < 2; ++role)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        qi[role][h] = k0 + g + 8 * h + lo + role;
-        const int ii = min(qi[role][h], N - 1);
-        lq[role][h] = __ldg(lse + ii) * kLog2e;
-        dd[role][h] = __ldg(dlt + ii);
+        const int i = k0 + g + 8 * h + lo + role;
+        const bool ok = (role == 0 || MODE == 1) && k0 + g + 8 * h <= j_last && i < N && i >= need;
+        v[role][h] = ok ? __ldg(pds + static_cast<size_t>(i) * stride + c) : make_float2(0.f, 0.f);
       }
     wait_stage(n);
     const unsigned char* qst = slot_of(n);
-    // role as a compile-time constant, so that nothing below is indexed at run time
-    auto do_role = [&](auto role_c) {
-      constexpr int role = decltype(role_c)::value;
-      bool ok[2];
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        ok[h] = !s_err && k0 + g + 8 * h <= j_last && qi[role][h] < N && qi[role][h] >= ks.need[c];
-      if (!__any_sync(0xffffffffu, ok[0] || ok[1])) return;  // uniform
-      // scores and dP against the query's rows r0 = j + role and (interp) r1 = j + role - 1;
-      // B fragments: column g of n-tile h = query of key k0 + g + 8h (slab row x)
-      float sc[2][2], dp[2][2];  // [row part][h]
-#pragma unroll
-      for (int part = 0; part < (MODE == 1 ? 2 : 1); ++part) {
-        const int off = role - part;
-        // S against K' rows, then dP against V' rows: one operand set live at a time
-        float C[2][4], E[2][4];
-#pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-          uint32_t aa[2][2][4];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int p = k0 + g + 8 * h + off;
-            lds_kfrag(own_row(kv, p), t, own_pos(p), aa[h][0], aa[h][1]);
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int x = min(16 * warp + g + 8 * h + role, xlast);
-            uint32_t bl[4], bh2[4];
-            lds_kfrag(reinterpret_cast<const uint4*>(qst + kv * kQ2 + x * kRowBytes), t, qfirst + x, bl, bh2);
-            float (&acc)[4] = kv == 0 ? C[h] : E[h];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) acc[u] = 0.f;
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-              mma16816(acc, aa[0][0][s], aa[1][0][s], aa[0][1][s], aa[1][1][s], bl[s], bh2[s]);
-          }
-        }
-        sc[part][0] = __shfl_sync(0xffffffffu, (g & 1) ? C[0][1] : C[0][0], src_lane);
-        sc[part][1] = __shfl_sync(0xffffffffu, (g & 1) ? C[1][3] : C[1][2], src_lane);
-        dp[part][0] = __shfl_sync(0xffffffffu, (g & 1) ? E[0][1] : E[0][0], src_lane);
-        dp[part][1] = __shfl_sync(0xffffffffu, (g & 1) ? E[1][3] : E[1][2], src_lane);
-      }
+    for (int role = 0; role < (MODE == 1 ? 2 : 1); ++role) {
+      if (role == 1 && !(w > 0.f)) continue;  // uniform: weight 0
       const float wt = MODE == 1 ? (role == 0 ? 1.f - w : w) : 1.f;
-      float xs[2], xp[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float sv = MODE == 1 ? (1.f - w) * sc[0][h] + w * sc[1][h] : sc[0][h];
-        const float dpp = MODE == 1 ? (1.f - w) * dp[0][h] + w * dp[1][h] : dp[0][h];
-        const float P = ok[h] ? exp2f(sv - lq[role][h]) : 0.f;
-        xs[h] = wt * P * (dpp - dd[role][h]);
-        xp[h] = wt * P;
-      }
-      // dk' += diag(wt dS) Q's[slab rows], dv += diag(wt P) dO'[slab rows]
-      const uint32_t s0 = pack_h2(xs[0] * sel_lo, xs[0] * sel_hi), s3 = pack_h2(xs[1] * sel_lo, xs[1] * sel_hi);
-      const uint32_t p0 = pack_h2(xp[0] * sel_lo, xp[0] * sel_hi), p3 = pack_h2(xp[1] * sel_lo, xp[1] * sel_hi);
+      const float xs0 = wt * v[role][0].y, xs1 = wt * v[role][1].y;
+      const float xp0 = wt * v[role][0].x, xp1 = wt * v[role][1].x;
+      if (!__any_sync(0xffffffffu, xs0 != 0.f || xs1 != 0.f || xp0 != 0.f || xp1 != 0.f)) continue;
+      const uint32_t s0 = pack_h2(xs0 * sel_lo, xs0 * sel_hi), s3 = pack_h2(xs1 * sel_lo, xs1 * sel_hi);
+      const uint32_t p0 = pack_h2(xp0 * sel_lo, xp0 * sel_hi), p3 = pack_h2(xp1 * sel_lo, xp1 * sel_hi);
       const int x = min(16 * warp + (mi & 1) * 8 + rl + role, xlast);
       const unsigned char* qrow = qst + x * kRowBytes;
       const int sw = swz(qfirst + x);
@@ -738,9 +643,7 @@ __global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
         mma16816(dV[nd], p0, 0u, 0u, p3, c4[0], c4[1]);
         mma16816(dV[nd + 1], p0, 0u, 0u, p3, c4[2], c4[3]);
       }
-    };
-    do_role(std::integral_constant<int, 0>{});
-    if (MODE == 1 && w > 0.f) do_role(std::integral_constant<int, 1>{});  // uniform: weight w
+    }
     release_stage(n);
   }
 
@@ -760,11 +663,12 @@ __global__ void __launch_bounds__(kBThreadsT, 2) bwd_kv_kernel(BtcArgs a) {
 // ------------------------------------------------------------------ launch
 bool bwd_tc_supported(const LayerTable& t) { return t.W <= 16; }
 
-size_t bwd_tc_workspace_bytes(int B, int H, int N) {
+size_t bwd_tc_workspace_bytes(int B, int H, int N, int W) {
   const size_t rows = static_cast<size_t>(B) * H * N;
   const size_t tiles = (static_cast<size_t>(N) + kBTileT - 1) / kBTileT * B * H;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  return 4 * up(rows * kRowBytes) + up(rows * sizeof(float)) + up(tiles * sizeof(float));
+  return 4 * up(rows * kRowBytes) + up(rows * sizeof(float)) + up(tiles * sizeof(float)) +
+         up(rows * (W + kMaxR) * sizeof(float2));
 }
 
 cudaError_t launch_dalpha_reduce(const float* partials, int n, float* dalpha, int mode, cudaStream_t stream);
@@ -788,7 +692,11 @@ cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   a.vp = reinterpret_cast<const __half*>(w + 3 * arr);
   float* delta = reinterpret_cast<float*>(w + 4 * arr);
   a.delta = delta;
+  const size_t tiles_all = static_cast<size_t>(a.tiles) * B * H;
   a.partials = reinterpret_cast<float*>(w + 4 * arr + up(static_cast<size_t>(rows) * sizeof(float)));
+  a.pds = reinterpret_cast<float2*>(w + 4 * arr + up(static_cast<size_t>(rows) * sizeof(float)) +
+                                    up(tiles_all * sizeof(float)));
+  a.pds_stride = t.W + t.n;  // the kernels keep at most t.n rungs
   a.lse = lse;
   a.dq = static_cast<__nv_bfloat16*>(dq);
   a.dk = static_cast<__nv_bfloat16*>(dk);
@@ -820,7 +728,7 @@ cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   a.slab_rows = kKvQRows;
   a.slot_bytes = 2 * kKvQRows * kRowBytes;
   {
-    const int smem = 2 * kKvOwn * kRowBytes + kBSlots * a.slot_bytes;
+    const int smem = kBSlots * a.slot_bytes;
     void (*kern)(BtcArgs) = t.mode == 0 ? bwd_kv_kernel<0> : bwd_kv_kernel<1>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
