@@ -133,6 +133,9 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const __nv_bfloat16* __res
   ko[(u + 4) ^ sw] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
   vo[u ^ sw] = make_uint4(za[0], za[1], za[2], za[3]);
   vo[(u + 4) ^ sw] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
+  // this thread's rows are written: the dependent attention grid may start launching (it
+  // waits for the whole of this grid before it reads K'/V')
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
 // ------------------------------------------------------------------ attention kernel
@@ -200,6 +203,9 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
         mbar_arrive_tx(&full_bar[slot], bytes);
         bulk_g2s(dst, Q + static_cast<size_t>(i0) * kD, bytes, &full_bar[slot]);
       } else if (n <= 2) {  // window rows [w0, i_last] of K' (n = 1) or V' (n = 2)
+        // K'/V' come from the preparation grid launched just before this one (programmatic
+        // dependent launch): wait for it, and its writes, before the first copy of them
+        if (n == 1) asm volatile("griddepcontrol.wait;\n" ::: "memory");
         const uint32_t bytes = static_cast<uint32_t>(i_last + 1 - w0) * kRowBytes;
         mbar_arrive_tx(&full_bar[slot], bytes);
         bulk_g2s(dst + (w0 - (i0 - 16)) * kRowBytes, (n == 1 ? Kp : Vp) + static_cast<size_t>(w0) * kD,
@@ -580,16 +586,23 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   const long long blocks = static_cast<long long>(a.tiles) * B * H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const int smem = kSlots * a.slot_bytes;
-  cudaError_t e;
-  if (t.mode == 0) {
-    e = cudaFuncSetAttribute(fwd_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    fwd_tc_kernel<0><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a);
-  } else {
-    e = cudaFuncSetAttribute(fwd_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    fwd_tc_kernel<1><<<static_cast<unsigned>(blocks), kTcThreads, smem, stream>>>(a);
-  }
+  void (*kern)(TcArgs) = t.mode == 0 ? fwd_tc_kernel<0> : fwd_tc_kernel<1>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  // programmatic dependent launch: the CTAs may start (build their key table, load and
+  // rotate Q) while the preceding preparation grid drains
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
