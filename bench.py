@@ -177,6 +177,32 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(use), "samples_inside_timed_region": len(inside)}
 
 
+# ----------------------------------------------------------------------------- ranks
+def barrier(world):
+    """All ranks meet here (a no-op for one process)."""
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world):
+    """The largest value of x over the ranks (x itself for one process): the job's time is
+    its slowest replica's.  Works on NCCL (a CUDA tensor) and gloo (a CPU tensor)."""
+    if world == 1:
+        return x
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.distributed.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank, world, ms):
+    """Whole-job throughput: every rank processes units_per_rank (weak scaling) in ms."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def setup(w, device):
     import torch
@@ -266,8 +292,7 @@ def time_device(w, steps, warmup, device, rank, world):
         for _ in range(warmup):
             graph.replay()
         torch.cuda.synchronize(device)
-        if world > 1:
-            torch.distributed.barrier()
+        barrier(world)
         clk.mark_start()
         with torch.cuda.stream(stream):
             e0.record(stream)
@@ -276,11 +301,7 @@ def time_device(w, steps, warmup, device, rank, world):
             e1.record(stream)
         torch.cuda.synchronize(device)
         clk.mark_end()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
     kpl = kernels_per_layer(wss)
     res = dict(ms_total=ms, ms_per_step=ms / steps, launches=kpl * w["L"] * steps, clocks=clk.summary())
     # end to end through the public API: pinned host inputs -> device -> 16 layers -> host O
@@ -307,11 +328,7 @@ def time_device(w, steps, warmup, device, rank, world):
             e2e_step()
         e1.record(stream)
     torch.cuda.synchronize(device)
-    ms_e2e = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_e2e], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
     res.update(ms_e2e_per_step=ms_e2e / e2e_steps, h2d=h2d, d2h=d2h, e2e_steps=e2e_steps,
                e2e_launches=kpl * w["L"] * e2e_steps)
     res["halves"] = time_halves(fa, torch, stream, device, plan, dev, outs, lses, adev, wss, steps, warmup)
@@ -455,8 +472,8 @@ def main():
 
     r = time_device(w, args.steps, args.warmup, device, rank, world)
     tokens_step = w["B"] * w["N"]
-    value = tokens_step * world / (r["ms_per_step"] / 1e3)
-    e2e_value = tokens_step * world / (r["ms_e2e_per_step"] / 1e3)
+    value = job_value(tokens_step, world, r["ms_per_step"])
+    e2e_value = job_value(tokens_step, world, r["ms_e2e_per_step"])
     peak, peak_kind = read_peaks()
     layer_s = r["ms_per_step"] / 1e3 / w["L"]
     # dominant kernel: the attention launch, timed alone (its algorithmic bytes are the
