@@ -61,7 +61,7 @@ constexpr int kTcMaxW = 16;
 #define FIB_TC_MIN_CTAS 4
 #endif
 #ifndef FIB_TC_MIN_CTAS_INTERP
-#define FIB_TC_MIN_CTAS_INTERP 3
+#define FIB_TC_MIN_CTAS_INTERP 4
 #endif
 constexpr int kSlots = FIB_TC_SLOTS;           // ring slots
 constexpr int kRungChunk = FIB_TC_CHUNK;       // rungs per online-softmax step
@@ -71,7 +71,7 @@ struct TcArgs {
   int N;
   int tiles;
   int bh;          // B * H
-  int slab_rows;   // rows of a rung slab region: 64 (mask) or 72 (interp: 65 used)
+  int slab_rows;   // rows of a rung slab region: 64 (mask) or 65 (interp)
   int slot_bytes;  // 2 * slab_rows * 128
   const __nv_bfloat16* q;
   const __half* kp;  // K' rows (prep_kv_kernel)
@@ -570,7 +570,7 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   a.N = N;
   a.tiles = (N + kTcTile - 1) / kTcTile;
   a.bh = B * H;
-  a.slab_rows = t.mode == 1 ? kTcTile + 8 : kTcTile;
+  a.slab_rows = t.mode == 1 ? kTcTile + 1 : kTcTile;  // interp reads one row more
   a.slot_bytes = 2 * a.slab_rows * kRowBytes;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.kp = static_cast<const __half*>(workspace);
