@@ -366,6 +366,33 @@ def time_backward(w, steps, warmup, device):
     return {"ms_per_step": ms, "us_per_layer": ms * 1e3 / w["L"]}
 
 
+def time_decode(mode, B, H, N, L, steps, warmup, device):
+    """One new token at position N-1 against an N-row cache, through the L layers of a
+    plan (Fibonacci base, alpha = 1.5, W = 12; interp takes alpha from the device as a
+    learned alpha would): microseconds per token, replayed from a CUDA graph."""
+    import torch
+    from fibonacci_offset_sparse_gb300 import fib_attn as fa
+    from fibonacci_offset_sparse_gb300 import inputs
+    m = fa.FIB_MODE_MASK if mode == "mask" else fa.FIB_MODE_INTERP
+    plan = fa.fib_attn_plan_create(fa.FIB_BASE_FIBONACCI, [1.5] * L, 12, N, m)
+    adev = torch.full((L,), 1.5, dtype=torch.float32, device=device) if mode == "interp" else None
+    caches = [tuple(t.to(device) for t in inputs.qkv(B, H, N, 64, 50, l, "bf16")[1:]) for l in range(L)]
+    qs = [inputs.normal((B, H, 64), 51, l, inputs.TENSOR_Q, "bf16").to(device) for l in range(L)]
+    outs = [torch.empty_like(q) for q in qs]
+    stream = torch.cuda.Stream(device)
+
+    def step():
+        for l in range(L):
+            fa.fib_attn_decode(plan, l, N - 1, qs[l], *caches[l], o=outs[l], alpha_dev=adev, want_lse=False)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize(device)
+    ms = time_graph(torch, stream, device, step, steps, warmup)
+    plan.close()
+    return ms * 1e3
+
+
 def time_dense_sdpa(w, device, reps=20):
     """Dense causal attention on the same shape through PyTorch's fused attention (a library
     kernel, timed only as the dense comparison point): milliseconds per layer."""
@@ -523,6 +550,10 @@ def main():
         wb = WORKLOADS[BACKWARD]
         rb = time_backward(wb, args.steps, args.warmup, device)
         bb = compulsory_bytes_bwd(wb)
+        dec = {m: time_decode(m, 1, 8, 4096, 16, args.steps, args.warmup, device) for m in ("mask", "interp")}
+        line["decode"] = {"shape": "B=1, H=8, 16 layers, cache N=4096, new token at 4095, W=12, alpha=1.5",
+                          "mask_us_per_token": dec["mask"], "interp_us_per_token": dec["interp"],
+                          "interp_over_mask": dec["interp"] / dec["mask"]}
         line["backward"] = {"workload": BACKWARD, "path": "interp backward (dQ, dK, dV, dalpha)",
                             "value": wb["B"] * wb["N"] * world / (rb["ms_per_step"] / 1e3), "unit": UNIT,
                             "ms_per_step": rb["ms_per_step"], "us_per_layer": rb["us_per_layer"],

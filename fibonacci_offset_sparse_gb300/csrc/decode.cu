@@ -6,15 +6,19 @@
 // the blend of rows pos-lo and pos-lo-1.  Key results 2 ("Efficiency") compares the
 // inference latency of the interpolated and the mask path; this kernel serves both.
 //
-// One warp per (b, h): its 8 quads take the W + R keys round-robin, each quad keeps its own
-// online softmax over the keys it saw (lane t of a quad holds the dims D_t, see
-// common.cuh), then the quads merge (max, rescale, sum) with shuffles.  RoPE is applied in
-// relative form from the factored tables, so the cache holds raw (unrotated) K rows.
+// One CTA of 32 quads per (b, h): quad c takes keys c, c+32, ... (every key of a usual
+// layer in one round), issuing all of its loads -- the RoPE factors, the K and V rows, the
+// partner rows of an interpolated key -- before it uses any, so that a decode step waits
+// for about one memory round trip.  Each quad keeps an online softmax over its keys (lane t
+// of a quad holds the dims D_t, see common.cuh); the 32 quads then merge through shared
+// memory in a fixed order (max, rescale, sum).  RoPE is applied in relative form from the
+// factored tables, so the cache holds raw (unrotated) K rows.
 #include "common.cuh"
 
 namespace fibattn {
 
-constexpr int kDecWarps = 4;
+constexpr int kDecQuads = 32;
+constexpr int kDecThreads = 4 * kDecQuads;
 
 struct DecArgs {
   LayerTable t;
@@ -45,21 +49,21 @@ __device__ __forceinline__ float rel_dot_reg(const float (&q)[16], const float (
 }
 
 template <typename DT>
-__global__ void __launch_bounds__(32 * kDecWarps) decode_kernel(DecArgs a) {
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(DecArgs a) {
   __shared__ KeySmem ks;
-  build_keys(a.t, a.N, &ks);
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x * kDecWarps + warp;
-  if (bh >= a.BH) return;  // whole warps only: the shuffles below stay full-warp
-  const int quad = lane >> 2, t = lane & 3;
+  __shared__ float s_m[kDecQuads], s_l[kDecQuads];
+  __shared__ float s_o[kDecQuads][kD];
+  const int bh = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int quad = tid >> 2, t = tid & 3;
   const int i = a.pos;
   const DT* Q = static_cast<const DT*>(a.q) + static_cast<size_t>(bh) * kD;
   const DT* K = static_cast<const DT*>(a.k) + static_cast<size_t>(bh) * a.N * kD;
   const DT* V = static_cast<const DT*>(a.v) + static_cast<size_t>(bh) * a.N * kD;
-
   float q[16];
-  load_part(Q, t, q);
+  load_part(Q, t, q);  // independent of the key table: in flight during its build
+  build_keys(a.t, a.N, &ks);
+  __syncthreads();
 #pragma unroll
   for (int u = 0; u < 16; ++u) q[u] *= kLog2e / 8.0f;
   float o[16];
@@ -67,69 +71,76 @@ __global__ void __launch_bounds__(32 * kDecWarps) decode_kernel(DecArgs a) {
   for (int u = 0; u < 16; ++u) o[u] = 0.f;
   float m = -INFINITY, l = 0.f;
   const int nv = ks.nv;
-  // every quad runs the same trip count, so the quad shuffles stay uniform
-  for (int c0 = 0; c0 < nv; c0 += 8) {
+  // the same trip count in every quad, so that the quad shuffles stay warp-uniform
+  for (int c0 = 0; c0 < nv; c0 += kDecQuads) {
     const int c = c0 + quad;
     const bool ok = c < nv && i >= ks.need[c];
-    float s = 0.f;
-    int lo = 0;
-    float w = 0.f;
+    const int lo = ok ? ks.lo[c] : 0;
+    const float w = ok ? ks.w[c] : 0.f;
+    const bool two = w > 0.f;
+    // every load of this key first: factors, K and V rows (and the partner rows)
+    float2 e0[8], e1[8];
+    float k0[16], k1[16], v0[16], v1[16];
     if (ok) {
-      lo = ks.lo[c];
-      w = ks.w[c];
-      float2 e[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) e[u] = rope_factor(a.rope_lo, a.rope_hi, lo, 8 * t + u);
-      float kx[16];
-      load_part(K + static_cast<size_t>(i - lo) * kD, t, kx);
-      s = rel_dot_reg(q, kx, e);
-      if (w > 0.f) {
+      for (int u = 0; u < 8; ++u) e0[u] = rope_factor(a.rope_lo, a.rope_hi, lo, 8 * t + u);
+      load_part(K + static_cast<size_t>(i - lo) * kD, t, k0);
+      load_part(V + static_cast<size_t>(i - lo) * kD, t, v0);
+      if (two) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) e[u] = rope_factor(a.rope_lo, a.rope_hi, lo + 1, 8 * t + u);
-        load_part(K + static_cast<size_t>(i - lo - 1) * kD, t, kx);
-        s = (1.f - w) * s + w * rel_dot_reg(q, kx, e);
+        for (int u = 0; u < 8; ++u) e1[u] = rope_factor(a.rope_lo, a.rope_hi, lo + 1, 8 * t + u);
+        load_part(K + static_cast<size_t>(i - lo - 1) * kD, t, k1);
+        load_part(V + static_cast<size_t>(i - lo - 1) * kD, t, v1);
       }
+    }
+    float s = 0.f;
+    if (ok) {
+      s = rel_dot_reg(q, k0, e0);
+      if (two) s = (1.f - w) * s + w * rel_dot_reg(q, k1, e1);
     }
     s = quad_sum(s);
-    if (ok) {
-      const float mn = fmaxf(m, s);
-      const float corr = exp2f(m - mn);
-      const float p = exp2f(s - mn);
-      l = l * corr + p;
-      float vx[16];
-      load_part(V + static_cast<size_t>(i - lo) * kD, t, vx);
-      const float p0 = p * (1.f - w);
+    if (!ok) continue;  // after the shuffles; no further warp-wide operation in this trip
+    const float mn = fmaxf(m, s);
+    const float corr = exp2f(m - mn);
+    const float p = exp2f(s - mn);
+    l = l * corr + p;
+    const float p0 = p * (1.f - w);
 #pragma unroll
-      for (int u = 0; u < 16; ++u) o[u] = fmaf(p0, vx[u], o[u] * corr);
-      if (w > 0.f) {
-        load_part(V + static_cast<size_t>(i - lo - 1) * kD, t, vx);
-        const float p1 = p * w;
+    for (int u = 0; u < 16; ++u) o[u] = fmaf(p0, v0[u], o[u] * corr);
+    if (two) {
+      const float p1 = p * w;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) o[u] = fmaf(p1, vx[u], o[u]);
-      }
-      m = mn;
+      for (int u = 0; u < 16; ++u) o[u] = fmaf(p1, v1[u], o[u]);
     }
+    m = mn;
   }
-  // merge the 8 quads (lanes with equal t hold the same dims)
-  float mall = m;
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) mall = fmaxf(mall, __shfl_xor_sync(0xffffffffu, mall, off));
+  // merge the quads in a fixed order: the largest max, then every quad rescaled to it
+  if (t == 0) s_m[quad] = m;
+  __syncthreads();
+  float mall = -INFINITY;
+  for (int qd = 0; qd < kDecQuads; ++qd) mall = fmaxf(mall, s_m[qd]);
   const float sc = (m == -INFINITY) ? 0.f : exp2f(m - mall);  // a quad that saw no key
-  l *= sc;
+  if (t == 0) s_l[quad] = l * sc;
+  // lane t holds dims [8t, 8t+8) in o[0..8) and [32+8t, 32+8t+8) in o[8..16)
 #pragma unroll
-  for (int u = 0; u < 16; ++u) o[u] *= sc;
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l += __shfl_xor_sync(0xffffffffu, l, off);
-#pragma unroll
-    for (int u = 0; u < 16; ++u) o[u] += __shfl_xor_sync(0xffffffffu, o[u], off);
+  for (int u = 0; u < 8; ++u) {
+    s_o[quad][8 * t + u] = o[u] * sc;
+    s_o[quad][32 + 8 * t + u] = o[8 + u] * sc;
   }
-  if (quad == 0) {
-    const float inv = 1.f / l;
-#pragma unroll
-    for (int u = 0; u < 16; ++u) o[u] *= inv;
-    store_part(static_cast<DT*>(a.o) + static_cast<size_t>(bh) * kD, t, o);
-    if (t == 0 && a.lse != nullptr) a.lse[bh] = (mall + log2f(l)) * kLn2;
+  __syncthreads();
+  if (tid < kD) {
+    float acc = 0.f, lsum = 0.f;
+    for (int qd = 0; qd < kDecQuads; ++qd) {
+      acc += s_o[qd][tid];
+      lsum += s_l[qd];
+    }
+    const float outv = acc / lsum;
+    if constexpr (sizeof(DT) == 4) {
+      static_cast<float*>(a.o)[static_cast<size_t>(bh) * kD + tid] = outv;
+    } else {
+      static_cast<__nv_bfloat16*>(a.o)[static_cast<size_t>(bh) * kD + tid] = __float2bfloat16_rn(outv);
+    }
+    if (tid == 0 && a.lse != nullptr) a.lse[bh] = (mall + log2f(lsum)) * kLn2;
   }
 }
 
@@ -148,11 +159,11 @@ cudaError_t launch_decode(const LayerTable& t, int B, int H, int N, int pos, int
   a.lse = lse;
   a.rope_lo = lo_tab;
   a.rope_hi = hi_tab;
-  const int blocks = (a.BH + kDecWarps - 1) / kDecWarps;
+  const int blocks = a.BH;
   if (dtype == 0)
-    decode_kernel<float><<<blocks, 32 * kDecWarps, 0, stream>>>(a);
+    decode_kernel<float><<<blocks, kDecThreads, 0, stream>>>(a);
   else
-    decode_kernel<__nv_bfloat16><<<blocks, 32 * kDecWarps, 0, stream>>>(a);
+    decode_kernel<__nv_bfloat16><<<blocks, kDecThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
