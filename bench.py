@@ -311,21 +311,46 @@ def time_device(w, steps, warmup, device, rank, world):
     d2h = sum(o.numel() * o.element_size() for o in o_host)
     e2e_steps = max(1, min(steps, 5))
 
-    def e2e_step():
+    # Per layer: host->device copy on one stream, the forward on `stream`, device->host copy
+    # of O on a third stream, so that layer l+1's copies overlap layer l's attention (the
+    # host buffers are pinned).  Events order each layer's buffers across steps.
+    h2d_stream, d2h_stream = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    L = len(pinned)
+    copied = [torch.cuda.Event() for _ in range(L)]
+    computed = [torch.cuda.Event() for _ in range(L)]
+    returned = [torch.cuda.Event() for _ in range(L)]
+    started = torch.cuda.Event()
+
+    def e2e_step(first):
         for l, (q, k, v) in enumerate(pinned):
-            dev[l][0].copy_(q, non_blocking=True)
-            dev[l][1].copy_(k, non_blocking=True)
-            dev[l][2].copy_(v, non_blocking=True)
-        run_stack(fa, plan, dev, outs, lses, adev, wss)
-        for l in range(len(outs)):
-            o_host[l].copy_(outs[l], non_blocking=True)
+            with torch.cuda.stream(h2d_stream):
+                h2d_stream.wait_event(started)
+                if not first:
+                    h2d_stream.wait_event(computed[l])  # the previous step is done with dev[l]
+                dev[l][0].copy_(q, non_blocking=True)
+                dev[l][1].copy_(k, non_blocking=True)
+                dev[l][2].copy_(v, non_blocking=True)
+                copied[l].record(h2d_stream)
+            stream.wait_event(copied[l])
+            if not first:
+                stream.wait_event(returned[l])  # the previous step's O of layer l is on the host
+            with torch.cuda.stream(stream):
+                fa.fib_attn_fwd(plan, l, *dev[l], o=outs[l], lse=lses[l], alpha_dev=adev, workspace=wss[l])
+                computed[l].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(computed[l])
+                o_host[l].copy_(outs[l], non_blocking=True)
+                returned[l].record(d2h_stream)
+        stream.wait_stream(d2h_stream)  # the step ends when every O is on the host
 
     with torch.cuda.stream(stream):
-        e2e_step()
+        started.record(stream)
+        e2e_step(True)
         torch.cuda.synchronize(device)
         e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
+        started.record(stream)
+        for s in range(e2e_steps):
+            e2e_step(False)
         e1.record(stream)
     torch.cuda.synchronize(device)
     ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
