@@ -385,10 +385,36 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   int srow[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) srow[h] = ic[h] - i0 + kI;
+  // ring slot and phase parity of the chunk's first stage, advanced as the loop runs (stage
+  // 3 + r sits in slot (3 + r) % kSlots, phase (3 + r) / kSlots)
+  int cslot = 3 % kSlots;
+  uint32_t cpar = (3 / kSlots) & 1;
+  auto advance = [&](int& sl, uint32_t& pr) {
+    if (++sl == kSlots) {
+      sl = 0;
+      pr ^= 1u;
+    }
+  };
+  const int vbase = 16 * warp + (mi & 1) * 8 + rl + kI;  // ldmatrix row of this lane, before clamping
   for (int r0 = 0; r0 < nrt; r0 += kRungChunk) {
+    int rsl[kRungChunk];
+    uint32_t rpr[kRungChunk];
+    {
+      int sl = cslot;
+      uint32_t pr = cpar;
+#pragma unroll
+      for (int cc = 0; cc < kRungChunk; ++cc) {
+        rsl[cc] = sl;
+        rpr[cc] = pr;
+        advance(sl, pr);
+      }
+    }
 #pragma unroll
     for (int cc = 0; cc < kRungChunk; ++cc)
-      if (r0 + cc < nrt) wait_stage(3 + r0 + cc);
+      if (r0 + cc < nrt && !s_err && !mbar_wait(&full_bar[rsl[cc]], rpr[cc], a.wait_ns)) {
+        s_err = 1;
+        atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
+      }
     float sc[2][kRungChunk];
     bool ok[2][kRungChunk], act[kRungChunk];
     int rowu[2][kRungChunk], first[kRungChunk], fcop[kRungChunk];
@@ -415,8 +441,8 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
       float C[kRungChunk][2][4];
 #pragma unroll
       for (int cc = 0; cc < kRungChunk; ++cc) {
-        const int r = r0 + cc < nrt ? r0 + cc : r0;
-        const uint4* kst = reinterpret_cast<const uint4*>(ring + ((3 + r) % kSlots) * a.slot_bytes);
+        const uint4* kst =
+            reinterpret_cast<const uint4*>(ring + (r0 + cc < nrt ? rsl[cc] : rsl[0]) * a.slot_bytes);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t kl[4], kh[4];
@@ -435,7 +461,8 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
           const int r = r0 + cc < nrt ? r0 + cc : r0;
           const float w = ks.w[W + r];
           if (w > 0.f) {  // uniform: w belongs to the rung
-            const uint4* kst = reinterpret_cast<const uint4*>(ring + ((3 + r) % kSlots) * a.slot_bytes);
+            const uint4* kst =
+                reinterpret_cast<const uint4*>(ring + (r0 + cc < nrt ? rsl[cc] : rsl[0]) * a.slot_bytes);
             float C2[2][4];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -490,7 +517,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
       if (!act[cc]) continue;  // uniform
       const int r = r0 + cc;
       const float w = MODE == 1 ? ks.w[W + r] : 0.f;
-      const unsigned char* vst = ring + ((3 + r) % kSlots) * a.slot_bytes + SR * kRowBytes;
+      const unsigned char* vst = ring + rsl[cc] * a.slot_bytes + SR * kRowBytes;
       float p[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -505,7 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
         const float x0 = p[0] * f, x1 = p[1] * f;
         const uint32_t a0 = pack_h2(x0 * sel_lo, x0 * sel_hi);
         const uint32_t a3 = pack_h2(x1 * sel_lo, x1 * sel_hi);
-        const int vr = min(max(16 * warp + (mi & 1) * 8 + rl + kI - part, fcop[cc]), lcop);
+        const int vr = min(max(vbase - part, fcop[cc]), lcop);
         const unsigned char* vrow = vst + vr * kRowBytes;
         const int sw = swz(first[cc] + vr);
 #pragma unroll
@@ -517,9 +544,12 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
         }
       }
     }
+    __syncwarp();
 #pragma unroll
-    for (int cc = 0; cc < kRungChunk; ++cc)
-      if (r0 + cc < nrt) release_stage(3 + r0 + cc);
+    for (int cc = 0; cc < kRungChunk; ++cc) {
+      if (r0 + cc < nrt && lane == 0) mbar_arrive(&empty_bar[rsl[cc]]);
+      advance(cslot, cpar);
+    }
   }
 
   // ---- epilogue (nothing is written after a wait gave up; the producer reports it)
