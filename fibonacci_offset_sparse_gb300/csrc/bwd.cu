@@ -272,11 +272,6 @@ __global__ void dalpha_reduce_kernel(const float* partials, int n, float* dalpha
   if (threadIdx.x == 0) *dalpha = mode == 1 ? red[0] : 0.f;
 }
 
-cudaError_t launch_dalpha_reduce(const float* partials, int n, float* dalpha, int mode, cudaStream_t stream) {
-  dalpha_reduce_kernel<<<1, 256, 0, stream>>>(partials, n, dalpha, mode);
-  return cudaGetLastError();
-}
-
 size_t bwd_workspace_bytes(int B, int H, int N) {
   const size_t rows = static_cast<size_t>(B) * H * N;
   const size_t tiles = (static_cast<size_t>(N) + kBTile - 1) / kBTile * B * H;

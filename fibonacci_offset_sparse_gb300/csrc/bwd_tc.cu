@@ -9,7 +9,7 @@
 //   dq_i = R(i)^T sum dS wt k'_j / 8      dk_j = R(j)^T sum dS wt q'_i / 8      dv_j = sum P wt dO_i
 // over the (query, key row) pairs with blend weight wt (1 for window and mask keys).
 //
-// Three launches (plus the fixed-order dalpha sum):
+// Three launches:
 //   * bwd_prep_kernel: Q's = RoPE(q) log2(e)/8, K' = RoPE(k), V' = v and dO' = dO, all f16
 //     with the chunk swizzle of fwd_tc.cu, and Delta (float32), each row read once.
 //   * bwd_q_kernel (query-owned, 64 queries a CTA): the forward's structure, with dP =
@@ -21,6 +21,7 @@
 //     recomputed.  The queries that read the CTA's keys stream through a ring (the 80-row
 //     block [j0, j0+80) of Q's and dO' for the window band, then per rung the query slab
 //     [j0+lo, j0+lo+65)); with their stored P and dS, dk' += dS^T Q's and dv += P^T dO'.
+//     Its CTA 0 also sums the dQ grid's dalpha partials in a fixed order.
 // Precision as the forward: f16 operands (Q's, K', V', dO', P, dS), f32 accumulation.
 #include <algorithm>
 #include <type_traits>
@@ -53,6 +54,8 @@ struct BtcArgs {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   float* partials;
+  int n_partials;   // CTAs of bwd_q_kernel
+  float* dalpha;    // written by bwd_kv_kernel's CTA 0: the fixed-order sum of the partials
   float2* pds;      // (P, dS) of every attended (query, key slot): [B*H*N][pds_stride]
   int pds_stride;   // W + rungs of the layer table
   const float2* rope_lo;
@@ -448,7 +451,10 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
     for (int wp = 0; wp < kBWarps; ++wp) s += red[wp];
     a.partials[blockIdx.x] = s;
   }
-  if (s_err) return;
+  if (s_err) {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    return;
+  }
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     if (irow[h] >= N) continue;
@@ -456,6 +462,9 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
     rope_natural(a.rope_lo, a.rope_hi, irow[h], t, e);
     store_rotated_back(a.dq + base + static_cast<size_t>(irow[h]) * kD, acc, h, t, e, 0.125f);
   }
+  // this thread's outputs (dq, P and dS, the partial) are written: the dependent kv grid may
+  // launch (it waits for this whole grid before it reads them)
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
 // ------------------------------------------------------------------ key-owned: dk, dv
@@ -499,6 +508,16 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
 
   // ===================================================================== producer
   if (warp == kBWarps) {
+    if (blockIdx.x == 0) {
+      // dalpha of the layer: the dQ grid's partials, summed in a fixed order (lane l takes
+      // partials l, l+32, ... in turn, then a fixed shuffle tree)
+      asm volatile("griddepcontrol.wait;\n" ::: "memory");
+      float acc = 0.f;
+      for (int idx = lane; idx < a.n_partials; idx += 32) acc += a.partials[idx];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (lane == 0) *a.dalpha = MODE == 1 ? acc : 0.f;
+    }
     if (lane != 0) return;
     int last_n[kBSlots];
 #pragma unroll
@@ -544,6 +563,9 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
     if (lane == 0) mbar_arrive(&empty_bar[n % kBSlots]);
   };
   auto slot_of = [&](int n) { return ring + (n % kBSlots) * a.slot_bytes; };
+  // P and dS come from the dQ grid launched just before (programmatic dependent launch):
+  // wait for it, and its writes, before the first load of them
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const float2* pds = a.pds + static_cast<size_t>(bh) * N * a.pds_stride;
   const int stride = a.pds_stride;
 
@@ -671,8 +693,6 @@ size_t bwd_tc_workspace_bytes(int B, int H, int N, int W) {
          up(rows * (W + kMaxR) * sizeof(float2));
 }
 
-cudaError_t launch_dalpha_reduce(const float* partials, int n, float* dalpha, int mode, cudaStream_t stream);
-
 cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k, const void* v,
                           const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
                           float* dalpha, void* ws, const float2* lo_tab, const float2* hi_tab, int* status,
@@ -724,19 +744,32 @@ cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* 
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(blocks), kBThreadsT, smem, stream>>>(a);
   }
-  // key-owned: dk, dv
+  // key-owned: dk, dv, and dalpha (CTA 0), launched as a programmatic dependent of the dQ
+  // grid: its prologue and first copies (of rows the preparation wrote) overlap that grid's
+  // tail; it waits for the grid before it reads P, dS and the partials
   a.slab_rows = kKvQRows;
   a.slot_bytes = 2 * kKvQRows * kRowBytes;
+  a.n_partials = static_cast<int>(blocks);
+  a.dalpha = dalpha;
   {
     const int smem = kBSlots * a.slot_bytes;
     void (*kern)(BtcArgs) = t.mode == 0 ? bwd_kv_kernel<0> : bwd_kv_kernel<1>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(blocks), kBThreadsT, smem, stream>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kBThreadsT);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) return e;
   }
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_dalpha_reduce(a.partials, static_cast<int>(blocks), dalpha, t.mode, stream);
+  return cudaGetLastError();
 }
 
 }  // namespace fibattn
