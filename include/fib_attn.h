@@ -51,7 +51,7 @@ typedef struct fib_attn_plan_s* fib_attn_plan_t;
 enum fib_status {
   FIB_OK = 0,
   FIB_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, out-of-range index   */
-  FIB_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (D != 64)  */
+  FIB_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement (D != 64) */
   FIB_ERR_CUDA = 3,          /* a CUDA runtime call failed (incl. no device)            */
   FIB_ERR_NOMEM = 4,         /* host or device allocation failed                        */
   FIB_ERR_TIMEOUT = 5,       /* a bounded device wait gave up (see last_device_status)  */
