@@ -122,6 +122,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        const float2* __restrict__ lo_tab,
                                                        const float2* __restrict__ hi_tab, int N, long long rows,
                                                        float qscale) {
+  // The dependent dQ grid may launch at once (its CTAs take the SMs as this single wave
+  // drains); it waits for the whole of this grid before it reads what this grid writes.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const long long gid = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
   const long long row = gid >> 2;
   const unsigned active = __ballot_sync(0xffffffffu, row < rows);  // whole quads
@@ -230,6 +233,9 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
       }
       unsigned char* dst = ring + slot * a.slot_bytes;
       if (n == 0) {  // Q's and dO' rows [i0, i_last]
+        // every array read from here on comes from the preparation grid launched just
+        // before this one (programmatic dependent launch): wait for it and its writes
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
         const uint32_t bytes = static_cast<uint32_t>(i_last - i0 + 1) * kRowBytes;
         mbar_arrive_tx(&full_bar[slot], 2 * bytes);
         bulk_g2s(dst, a.qs + base + static_cast<size_t>(i0) * kD, bytes, &full_bar[slot]);
@@ -267,6 +273,7 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
   const int q0 = i0 + 16 * warp;
   int irow[2], ic[2];
   float lse2[2], dlt[2];
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");  // Delta comes from the preparation grid
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     irow[h] = q0 + g + 8 * h;
@@ -738,15 +745,29 @@ cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   a.slab_rows = t.mode == 1 ? kBTileT + 8 : kBTileT;
   a.slot_bytes = 2 * a.slab_rows * kRowBytes;
   {
+    // a programmatic dependent of the preparation grid: the CTAs' prologue overlaps its tail
     const int smem = kBSlots * a.slot_bytes;
     void (*kern)(BtcArgs) = t.mode == 0 ? bwd_q_kernel<0> : bwd_q_kernel<1>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(blocks), kBThreadsT, smem, stream>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kBThreadsT);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) return e;
   }
   // key-owned: dk, dv, and dalpha (CTA 0), launched as a programmatic dependent of the dQ
   // grid: its prologue and first copies (of rows the preparation wrote) overlap that grid's
-  // tail; it waits for the grid before it reads P, dS and the partials
+  // tail; it waits for the grid before it reads P, dS and the partials.  The dQ CTAs signal
+  // only at their end, after each of their threads waited for the preparation grid, so that
+  // grid has completed before this one launches.
   a.slab_rows = kKvQRows;
   a.slot_bytes = 2 * kKvQRows * kRowBytes;
   a.n_partials = static_cast<int>(blocks);

@@ -99,6 +99,10 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const __nv_bfloat16* __res
                                                       const float2* __restrict__ lo_tab,
                                                       const float2* __restrict__ hi_tab, int N,
                                                       long long rows) {
+  // The dependent attention grid may launch at once: its CTAs take the SMs as this single
+  // wave drains and load and rotate their Q rows meanwhile; each waits for the whole of this
+  // grid (griddepcontrol.wait) before it reads K'/V'.
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const long long gid = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
   const long long row = gid >> 2;
   if (row >= rows) return;
@@ -133,9 +137,6 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const __nv_bfloat16* __res
   ko[(u + 4) ^ sw] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
   vo[u ^ sw] = make_uint4(za[0], za[1], za[2], za[3]);
   vo[(u + 4) ^ sw] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
-  // this thread's rows are written: the dependent attention grid may start launching (it
-  // waits for the whole of this grid before it reads K'/V')
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
 // ------------------------------------------------------------------ attention kernel
