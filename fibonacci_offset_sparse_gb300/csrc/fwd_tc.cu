@@ -165,15 +165,20 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   const int i_last = min(i0 + kTcTile, N) - 1;  // last real query of the tile
   const int w0 = max(i0 - 16, 0);                // first copied window row
 
-  build_keys(a.t, N, &ks);
-  if (tid == 0) {
+  // The producer lane initialises the mbarriers and issues stage 0 (the Q rows, an input of
+  // this grid) before the block barrier, so that the copy overlaps the key-table build.
+  if (tid == kConsumers) {
     s_err = 0;
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kTcWarps);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    const uint32_t bytes = static_cast<uint32_t>(i_last - i0 + 1) * kRowBytes;
+    mbar_arrive_tx(&full_bar[0], bytes);
+    bulk_g2s(ring, Q + static_cast<size_t>(i0) * kD, bytes, &full_bar[0]);
   }
+  build_keys(a.t, N, &ks);
   __syncthreads();  // the only block-wide barrier: the roles split below
   const int W = a.t.W;
   const int nr = ks.nr;
@@ -191,7 +196,8 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
     int last_n[kSlots];
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) last_n[s] = -1;
-    for (int n = 0; n < n_stages; ++n) {
+    last_n[0] = 0;  // stage 0 was issued before the block barrier
+    for (int n = 1; n < n_stages; ++n) {
       if (s_err) break;
       const int slot = n % kSlots;
       if (!mbar_wait_backoff(&empty_bar[slot], ((n / kSlots) & 1) ^ 1, a.wait_ns)) {
@@ -199,11 +205,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
         break;
       }
       unsigned char* dst = ring + slot * a.slot_bytes;
-      if (n == 0) {  // Q rows [i0, i_last]
-        const uint32_t bytes = static_cast<uint32_t>(i_last - i0 + 1) * kRowBytes;
-        mbar_arrive_tx(&full_bar[slot], bytes);
-        bulk_g2s(dst, Q + static_cast<size_t>(i0) * kD, bytes, &full_bar[slot]);
-      } else if (n <= 2) {  // window rows [w0, i_last] of K' (n = 1) or V' (n = 2)
+      if (n <= 2) {  // window rows [w0, i_last] of K' (n = 1) or V' (n = 2)
         // K'/V' come from the preparation grid launched just before this one (programmatic
         // dependent launch): wait for it, and its writes, before the first copy of them
         if (n == 1) asm volatile("griddepcontrol.wait;\n" ::: "memory");
