@@ -25,7 +25,8 @@ cudaError_t launch_prep_kv(int B, int H, int N, const void* k, const void* v, co
                            const float2* hi_tab, void* workspace, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* workspace,
                           void* o, float* lse, const float2* lo_tab, const float2* hi_tab, int* status,
-                          unsigned long long wait_ns, int skip_first_rung_copy, cudaStream_t stream);
+                          unsigned long long wait_ns, int skip_first_rung_copy, bool after_prep,
+                          cudaStream_t stream);
 cudaError_t launch_debug_indices(const LayerTable& t, int N, int i0, int i1, int32_t* out,
                                  float* w_out, cudaStream_t stream);
 size_t bwd_workspace_bytes(int B, int H, int N);
@@ -328,7 +329,7 @@ int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, c
     const cudaError_t e = launch_prep_kv(B, H, N, k, v, p->d_lo, p->d_hi, workspace, s);
     if (e != cudaSuccess) return cuda_status(e);
     return cuda_status(launch_fwd_tc(t, B, H, N, q, workspace, o, lse, p->d_lo, p->d_hi, p->d_status,
-                                     p->wait_ns, p->skip_first_rung_copy, s));
+                                     p->wait_ns, p->skip_first_rung_copy, true, s));
   }
   return cuda_status(launch_fwd(t, B, H, N, dtype, q, k, v, o, lse, p->d_lo, p->d_hi,
                                 static_cast<cudaStream_t>(stream)));
@@ -367,7 +368,7 @@ int fib_attn_fwd_attend(fib_attn_plan_t p, int layer, int B, int H, int N, int d
   st = make_table(p, layer, N, p->mode == FIB_MODE_INTERP ? alpha_dev : nullptr, &t);
   if (st != FIB_OK) return st;
   return cuda_status(launch_fwd_tc(t, B, H, N, q, workspace, o, lse, p->d_lo, p->d_hi, p->d_status,
-                                   p->wait_ns, p->skip_first_rung_copy,
+                                   p->wait_ns, p->skip_first_rung_copy, false,
                                    static_cast<cudaStream_t>(stream)));
 }
 

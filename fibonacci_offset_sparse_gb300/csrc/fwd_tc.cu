@@ -54,9 +54,6 @@ constexpr int kTcMaxW = 16;
 #ifndef FIB_TC_SLOTS
 #define FIB_TC_SLOTS 3
 #endif
-#ifndef FIB_TC_CHUNK
-#define FIB_TC_CHUNK 1
-#endif
 #ifndef FIB_TC_MIN_CTAS
 #define FIB_TC_MIN_CTAS 4
 #endif
@@ -64,7 +61,6 @@ constexpr int kTcMaxW = 16;
 #define FIB_TC_MIN_CTAS_INTERP 4
 #endif
 constexpr int kSlots = FIB_TC_SLOTS;           // ring slots
-constexpr int kRungChunk = FIB_TC_CHUNK;       // rungs per online-softmax step
 
 struct TcArgs {
   LayerTable t;
@@ -344,7 +340,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
         sum += s;
       }
     lw[h] = sum;  // lane-partial window sum
-    lr[h] = 0.f;  // rung sum (the same in the 4 lanes of a quad)
+    lr[h] = 0.f;  // rung sum (nonzero in the holder lane of the quad only)
   }
   // ---- window: O = P V'.  ldmatrix lane l supplies row (l&7) of matrix l>>3: keys
   // 16 s2 + 8 ((l>>3)&1) + (l&7), chunk nd + (l>>4).  Rows outside [w0, i_last] (P = 0 there)
@@ -373,135 +369,105 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   }
   release_stage(2);
 
-  // ---- rungs: chunks of kRungChunk, online softmax; rung r is stage 3 + r.
+  // ---- rungs: one per online-softmax step; rung r is stage 3 + r.
   // Slab row of query i: i - i0 + kI (global row i - lo; interp: its partner i - lo - 1 is
   // the row before).  Rows that a query does not attend are read from the slab's first
-  // copied row (finite data) and get p = 0; a warp none of whose rows attends either rung
-  // of a chunk skips it as a whole (a uniform branch).
-  // Diagonal pick: query g's score sits in lane (g, g>>1) of key n-tile 0, element g&1; query
-  // g+8's in the same lane of n-tile 1, element 2 + (g&1).  That lane also holds the nonzero
-  // entries of A = diag(P): row g in a0, row g+8 in a3, each in half g&1.
+  // copied row (finite data) and get p = 0; a warp none of whose rows attends a rung skips
+  // it as a whole (a uniform branch).
+  // Diagonal: query g's score sits in lane (g, g>>1) of key n-tile 0, element g&1; query
+  // g+8's in the same lane of n-tile 1, element 2 + (g&1).  Only that "holder" lane keeps a
+  // rung's score (the other three take -inf, so p = 0 there), and it holds the nonzero
+  // entries of A = diag(P) as well: row g in a0, row g+8 in a3, each in half g&1.  So the
+  // rung part of the softmax sum accumulates in the holder lane and joins the quad sum at
+  // the end, and the reference m, the same in the four lanes of a quad, moves only through
+  // a rescale that broadcasts the holder's value.
+  const bool holder = t == (g >> 1);
   const int src_lane = 4 * g + (g >> 1);
-  const float sel_lo = (t == (g >> 1) && !(g & 1)) ? 1.f : 0.f;
-  const float sel_hi = (t == (g >> 1) && (g & 1)) ? 1.f : 0.f;
   const int lcop = i_last - i0 + kI;  // last copied slab row of every rung
   int srow[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) srow[h] = ic[h] - i0 + kI;
-  // ring slot and phase parity of the chunk's first stage, advanced as the loop runs (stage
-  // 3 + r sits in slot (3 + r) % kSlots, phase (3 + r) / kSlots)
-  int cslot = 3 % kSlots;
-  uint32_t cpar = (3 / kSlots) & 1;
-  auto advance = [&](int& sl, uint32_t& pr) {
-    if (++sl == kSlots) {
-      sl = 0;
-      pr ^= 1u;
-    }
-  };
+  // ring slot and phase parity of the current stage (stage 3 + r sits in slot (3 + r) %
+  // kSlots, phase (3 + r) / kSlots), advanced as the loop runs
+  int slot = 3 % kSlots;
+  uint32_t par = (3 / kSlots) & 1;
   const int vbase = 16 * warp + (mi & 1) * 8 + rl + kI;  // ldmatrix row of this lane, before clamping
-  for (int r0 = 0; r0 < nrt; r0 += kRungChunk) {
-    int rsl[kRungChunk];
-    uint32_t rpr[kRungChunk];
-    {
-      int sl = cslot;
-      uint32_t pr = cpar;
+  // A rung's metadata does not depend on the staged rows: it is computed for the next rung
+  // while the current rung's products are in flight.
+  int first = 0, fcop = 0, rowu[2] = {0, 0};
+  bool ok[2] = {false, false}, act = false;
+  float wr = 0.f;
+  auto meta = [&](int r) {
+    const int c = W + r;
+    const int lo = ks.lo[c];
+    const int need = ks.need[c];
+    first = i0 - lo - kI;          // global row of slab row 0
+    fcop = max(0, lo - i0 + kI);   // first copied slab row (<= lcop: the tile attends r)
 #pragma unroll
-      for (int cc = 0; cc < kRungChunk; ++cc) {
-        rsl[cc] = sl;
-        rpr[cc] = pr;
-        advance(sl, pr);
-      }
+    for (int h = 0; h < 2; ++h) {
+      ok[h] = ic[h] >= need;
+      rowu[h] = ok[h] ? srow[h] : fcop;
     }
-#pragma unroll
-    for (int cc = 0; cc < kRungChunk; ++cc)
-      if (r0 + cc < nrt && !s_err && !mbar_wait(&full_bar[rsl[cc]], rpr[cc], a.wait_ns)) {
-        s_err = 1;
-        atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
-      }
-    float sc[2][kRungChunk];
-    bool ok[2][kRungChunk], act[kRungChunk];
-    int rowu[2][kRungChunk], first[kRungChunk], fcop[kRungChunk];
-#pragma unroll
-    for (int cc = 0; cc < kRungChunk; ++cc) {
-      const int r = r0 + cc < nrt ? r0 + cc : r0;  // a chunk past the end repeats rung r0, masked
-      const int c = W + r;
-      const int lo = ks.lo[c];
-      const bool in = (r0 + cc < nrt) && !s_err;
-      first[cc] = i0 - lo - kI;             // global row of slab row 0
-      fcop[cc] = max(0, lo - i0 + kI);      // first copied slab row (<= lcop: the tile attends r)
+    act = __any_sync(0xffffffffu, ok[0] || ok[1]);
+    if (MODE == 1) wr = ks.w[c];
+  };
+  if (nrt > 0) meta(0);
+  for (int r = 0; r < nrt; ++r) {
+    if (!s_err && !mbar_wait(&full_bar[slot], par, a.wait_ns)) {
+      s_err = 1;
+      atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
+    }
+    const unsigned char* st = ring + slot * a.slot_bytes;
+    float sc[2] = {-INFINITY, -INFINITY};
+    if (act) {  // uniform
+      const uint4* kst = reinterpret_cast<const uint4*>(st);
+      float d[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        ok[h][cc] = in && ic[h] >= ks.need[c];
-        rowu[h][cc] = ok[h][cc] ? srow[h] : fcop[cc];
-        sc[h][cc] = -INFINITY;
-      }
-      act[cc] = __any_sync(0xffffffffu, ok[0][cc] || ok[1][cc]);
-    }
-    bool any_act = false;
-#pragma unroll
-    for (int cc = 0; cc < kRungChunk; ++cc) any_act |= act[cc];
-    if (any_act) {  // uniform; the chunk's MMAs in one block, free to overlap
-      float C[kRungChunk][2][4];
-#pragma unroll
-      for (int cc = 0; cc < kRungChunk; ++cc) {
-        const uint4* kst =
-            reinterpret_cast<const uint4*>(ring + (r0 + cc < nrt ? rsl[cc] : rsl[0]) * a.slot_bytes);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t kl[4], kh[4];
-          lds_kfrag(kst + rowu[h][cc] * 8, t, first[cc] + rowu[h][cc], kl, kh);
-          C[cc][h][0] = C[cc][h][1] = C[cc][h][2] = C[cc][h][3] = 0.f;
+        uint32_t kl[4], kh[4];
+        lds_kfrag(kst + rowu[h] * 8, t, first + rowu[h], kl, kh);
+        if (MODE == 0) {
+          // two independent halves of the k-sum: MMA dependency chains of two, not four
+          float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+          mma16816(ca, qa[0][0][0], qa[1][0][0], qa[0][1][0], qa[1][1][0], kl[0], kh[0]);
+          mma16816(cb, qa[0][0][2], qa[1][0][2], qa[0][1][2], qa[1][1][2], kl[2], kh[2]);
+          mma16816(ca, qa[0][0][1], qa[1][0][1], qa[0][1][1], qa[1][1][1], kl[1], kh[1]);
+          mma16816(cb, qa[0][0][3], qa[1][0][3], qa[0][1][3], qa[1][1][3], kl[3], kh[3]);
+          d[h] = (g & 1) ? ca[2 * h + 1] + cb[2 * h + 1] : ca[2 * h] + cb[2 * h];
+        } else {  // (interp keeps registers for its second row)
+          float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int s = 0; s < 4; ++s)
-            mma16816(C[cc][h], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
+            mma16816(c, qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
+          d[h] = (g & 1) ? c[2 * h + 1] : c[2 * h];
         }
       }
+      if (MODE == 1 && wr > 0.f) {  // uniform: w belongs to the rung
+        float C2[2][4];
 #pragma unroll
-      for (int cc = 0; cc < kRungChunk; ++cc) {
-        float d0 = (g & 1) ? C[cc][0][1] : C[cc][0][0];
-        float d1 = (g & 1) ? C[cc][1][3] : C[cc][1][2];
-        if (MODE == 1) {
-          const int r = r0 + cc < nrt ? r0 + cc : r0;
-          const float w = ks.w[W + r];
-          if (w > 0.f) {  // uniform: w belongs to the rung
-            const uint4* kst =
-                reinterpret_cast<const uint4*>(ring + (r0 + cc < nrt ? rsl[cc] : rsl[0]) * a.slot_bytes);
-            float C2[2][4];
+        for (int h = 0; h < 2; ++h) {
+          const int row = max(rowu[h] - 1, fcop);
+          uint32_t kl[4], kh[4];
+          lds_kfrag(kst + row * 8, t, first + row, kl, kh);
+          C2[h][0] = C2[h][1] = C2[h][2] = C2[h][3] = 0.f;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int row = max(rowu[h][cc] - 1, fcop[cc]);
-              uint32_t kl[4], kh[4];
-              lds_kfrag(kst + row * 8, t, first[cc] + row, kl, kh);
-              C2[h][0] = C2[h][1] = C2[h][2] = C2[h][3] = 0.f;
-#pragma unroll
-              for (int s = 0; s < 4; ++s)
-                mma16816(C2[h], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
-            }
-            d0 = (1.f - w) * d0 + w * ((g & 1) ? C2[0][1] : C2[0][0]);
-            d1 = (1.f - w) * d1 + w * ((g & 1) ? C2[1][3] : C2[1][2]);
-          }
+          for (int s = 0; s < 4; ++s)
+            mma16816(C2[h], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
         }
-        d0 = __shfl_sync(0xffffffffu, d0, src_lane);
-        d1 = __shfl_sync(0xffffffffu, d1, src_lane);
-        sc[0][cc] = ok[0][cc] ? d0 : -INFINITY;
-        sc[1][cc] = ok[1][cc] ? d1 : -INFINITY;
+        d[0] = (1.f - wr) * d[0] + wr * ((g & 1) ? C2[0][1] : C2[0][0]);
+        d[1] = (1.f - wr) * d[1] + wr * ((g & 1) ? C2[1][3] : C2[1][2]);
       }
+      sc[0] = holder && ok[0] ? d[0] : -INFINITY;
+      sc[1] = holder && ok[1] ? d[1] : -INFINITY;
     }
     // Online softmax with a lazy reference: m only moves when a score passes it by more
     // than 8 (log2 units), so p = 2^(s - m) <= 256 (exact in f16 range) and O and the sums
     // are rescaled only then.
-    bool grow = false;
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int cc = 0; cc < kRungChunk; ++cc) grow |= sc[h][cc] > m[h] + 8.f;
-    if (__any_sync(0xffffffffu, grow)) {  // uniform
+    if (__any_sync(0xffffffffu, sc[0] > m[0] + 8.f || sc[1] > m[1] + 8.f)) {  // uniform
       float corr[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        float mc = m[h];
-#pragma unroll
-        for (int cc = 0; cc < kRungChunk; ++cc) mc = fmaxf(mc, sc[h][cc]);
+        const float mc = __shfl_sync(0xffffffffu, fmaxf(m[h], sc[h]), src_lane);
         corr[h] = exp2f(m[h] - mc);
         m[h] = mc;
         lw[h] *= corr[h];
@@ -515,29 +481,25 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
         O[nt][3] *= corr[1];
       }
     }
-#pragma unroll
-    for (int cc = 0; cc < kRungChunk; ++cc) {
-      if (!act[cc]) continue;  // uniform
-      const int r = r0 + cc;
-      const float w = MODE == 1 ? ks.w[W + r] : 0.f;
-      const unsigned char* vst = ring + rsl[cc] * a.slot_bytes + SR * kRowBytes;
+    if (act) {  // uniform
+      const unsigned char* vst = st + SR * kRowBytes;
       float p[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        p[h] = exp2f(sc[h][cc] - m[h]);  // 0 for a row that does not attend
+        p[h] = exp2f(sc[h] - m[h]);  // 0 outside the holder lanes and for rows that do not attend
         lr[h] += p[h];
       }
       // O += diag(p (1-w)) V'[slab rows of the 16 queries]; interp: + diag(p w) V'[rows - 1]
 #pragma unroll
       for (int part = 0; part < (MODE == 1 ? 2 : 1); ++part) {
-        if (part == 1 && !(w > 0.f)) break;  // uniform
-        const float f = MODE == 1 ? (part == 0 ? 1.f - w : w) : 1.f;
+        if (part == 1 && !(wr > 0.f)) break;  // uniform
+        const float f = MODE == 1 ? (part == 0 ? 1.f - wr : wr) : 1.f;
         const float x0 = p[0] * f, x1 = p[1] * f;
-        const uint32_t a0 = pack_h2(x0 * sel_lo, x0 * sel_hi);
-        const uint32_t a3 = pack_h2(x1 * sel_lo, x1 * sel_hi);
-        const int vr = min(max(vbase - part, fcop[cc]), lcop);
+        const uint32_t a0 = (g & 1) ? pack_h2(0.f, x0) : pack_h2(x0, 0.f);
+        const uint32_t a3 = (g & 1) ? pack_h2(0.f, x1) : pack_h2(x1, 0.f);
+        const int vr = min(max(vbase - part, fcop), lcop);
         const unsigned char* vrow = vst + vr * kRowBytes;
-        const int sw = swz(first[cc] + vr);
+        const int sw = swz(first + vr);
 #pragma unroll
         for (int nd = 0; nd < 8; nd += 2) {
           uint32_t b[4];
@@ -548,10 +510,11 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
       }
     }
     __syncwarp();
-#pragma unroll
-    for (int cc = 0; cc < kRungChunk; ++cc) {
-      if (r0 + cc < nrt && lane == 0) mbar_arrive(&empty_bar[rsl[cc]]);
-      advance(cslot, cpar);
+    if (lane == 0) mbar_arrive(&empty_bar[slot]);
+    if (r + 1 < nrt) meta(r + 1);  // uniform
+    if (++slot == kSlots) {
+      slot = 0;
+      par ^= 1u;
     }
   }
 
@@ -559,10 +522,9 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   if (s_err) return;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    float l = lw[h];
+    float l = lw[h] + lr[h];  // lane partial: its window terms, and the rung terms in the holder
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
-    l += lr[h];
     const int i = irow[h];
     if (i < N) {
       const float inv = 1.f / l;
@@ -596,7 +558,8 @@ cudaError_t launch_prep_kv(int B, int H, int N, const void* k, const void* v, co
 
 cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* workspace,
                           void* o, float* lse, const float2* lo_tab, const float2* hi_tab, int* status,
-                          unsigned long long wait_ns, int skip_first_rung_copy, cudaStream_t stream) {
+                          unsigned long long wait_ns, int skip_first_rung_copy, bool after_prep,
+                          cudaStream_t stream) {
   const long long rows = static_cast<long long>(B) * H * N;
   TcArgs a;
   a.t = t;
@@ -622,8 +585,11 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   void (*kern)(TcArgs) = t.mode == 0 ? fwd_tc_kernel<0> : fwd_tc_kernel<1>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  // programmatic dependent launch: the CTAs may start (build their key table, load and
-  // rotate Q) while the preceding preparation grid drains
+  // After this layer's own preparation grid (after_prep) the launch is a programmatic
+  // dependent of it: the CTAs may start (build their key table, load and rotate Q) while
+  // that grid drains, and wait for it before they read K'/V'.  Q is read before that wait,
+  // which is safe only because the preparation writes nothing but the workspace; after any
+  // other grid (the split entry point) the launch is an ordinary one.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kTcThreads);
@@ -633,7 +599,7 @@ cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = after_prep ? 1 : 0;
   e = cudaLaunchKernelEx(&cfg, kern, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
