@@ -10,11 +10,15 @@
 //     here replaces a rotation and a conversion per (query, rung) in the attention kernel.
 //   * fwd_tc_kernel: a CTA owns 64 consecutive queries of one (b,h): 4 compute warps of 16
 //     queries plus one producer thread that streams the rows they read through a 3-slot
-//     shared-memory ring with cp.async.bulk (mbarrier completion): the Q rows, the window
-//     rows [i0-16, i0+64) of K' and V', then per rung the slab rows [i0-d, i0-d+64) of K'
-//     and V'.  The producer refills a slot once the 4 compute warps release it; with one
-//     rung per online-softmax step the next two stages are in flight while a rung is being
-//     computed.  3 slots of 16 KB and 96 registers a thread let 4 CTAs share an SM.  Every
+//     shared-memory ring with cp.async.bulk (mbarrier completion): the Q rows, the "near
+//     block" rows [i0-64, i0+64) of K' and of V', then per remaining rung the slab rows
+//     [i0-d, i0-d+64) of K' and V'.  The near block holds the window band and the slab of
+//     every rung with d <= 64 (up to 5 or 6 of them), so those rungs need no copy of their
+//     own and are computed together with the window.  The producer refills a slot once the
+//     4 compute warps release it; with one streamed rung per online-softmax step the next
+//     two stages are in flight while a rung is being computed.  The producer issues the Q
+//     copy before the block barrier.  3 slots of 16 KB and 96 registers a thread let 4 CTAs
+//     share an SM.  Every
 //     mbarrier wait is bounded in time; a wait that gives up records FIB_ERR_TIMEOUT in the
 //     plan's status word, the warps stop, and the producer lets its copies in flight land
 //     before the CTA exits.
@@ -61,6 +65,8 @@ constexpr int kTcMaxW = 16;
 #define FIB_TC_MIN_CTAS_INTERP 4
 #endif
 constexpr int kSlots = FIB_TC_SLOTS;           // ring slots
+constexpr int kNear = 64;     // the near block holds K'/V' rows [i0 - kNear, i0 + 64)
+
 
 struct TcArgs {
   LayerTable t;
@@ -184,7 +190,12 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   // that some row of it attends (a later tile attends more).
   const unsigned attended = __ballot_sync(0xffffffffu, lane < nr && ks.need[W + lane] <= i_last);
   const int nrt = 32 - __clz(static_cast<int>(attended));
-  const int n_stages = 3 + nrt;  // Q, window K', window V', then one per streamed rung
+  // Rungs whose slab lies inside the near block (ascending distances: a prefix) are served
+  // from it, up to kMaxNear of them (per path, the largest count whose score registers fit
+  // the 96-register budget without spilling); every other rung streams its own slab.
+  constexpr int kMaxNear = MODE == 0 ? 5 : 6;
+  const int n_near = min(kMaxNear, __popc(__ballot_sync(0xffffffffu, lane < nrt && ks.lo[W + lane] + kI <= kNear)));
+  const int n_stages = 3 + nrt - n_near;  // Q, near K', near V', then one per streamed rung
 
   // ===================================================================== producer
   if (warp == kTcWarps) {
@@ -201,17 +212,18 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
         break;
       }
       unsigned char* dst = ring + slot * a.slot_bytes;
-      if (n <= 2) {  // window rows [w0, i_last] of K' (n = 1) or V' (n = 2)
+      if (n <= 2) {  // near-block rows [nb0, i_last] of K' (n = 1) or V' (n = 2)
         // K'/V' come from the preparation grid launched just before this one (programmatic
         // dependent launch): wait for it, and its writes, before the first copy of them
         if (n == 1) asm volatile("griddepcontrol.wait;\n" ::: "memory");
-        const uint32_t bytes = static_cast<uint32_t>(i_last + 1 - w0) * kRowBytes;
+        if (n == 2 && a.skip_first_rung_copy) continue;  // test hook: this stage never completes
+        const int nb0 = max(i0 - kNear, 0);
+        const uint32_t bytes = static_cast<uint32_t>(i_last + 1 - nb0) * kRowBytes;
         mbar_arrive_tx(&full_bar[slot], bytes);
-        bulk_g2s(dst + (w0 - (i0 - 16)) * kRowBytes, (n == 1 ? Kp : Vp) + static_cast<size_t>(w0) * kD,
+        bulk_g2s(dst + (nb0 - (i0 - kNear)) * kRowBytes, (n == 1 ? Kp : Vp) + static_cast<size_t>(nb0) * kD,
                  bytes, &full_bar[slot]);
       } else {  // rung slab: rows [first, first + SR) of K', then of V', where inside [0, N)
-        const int r = n - 3;
-        if (r == 0 && a.skip_first_rung_copy) continue;  // test hook: this stage never completes
+        const int r = n_near + n - 3;
         const int lo = ks.lo[W + r];
         const int first = i0 - lo - kI;
         const int r0 = max(first, 0);
@@ -293,87 +305,17 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   }
   release_stage(0);
 
-  // ---- window: S = Q' K'^T over keys [q0-16, q0+16) (slot row r holds position i0-16+r;
-  // rows outside [w0, i_last] hold stale data: their scores are masked below)
+  // ---- near block: K'/V' rows [i0 - kNear, i0 + 64) (index = position - (i0 - kNear); rows
+  // outside [max(i0 - kNear, 0), i_last] hold stale data and are masked or clamped below).
+  // It serves the window band and the first n_near rungs in the same two stages.
   const uint4* Ks = reinterpret_cast<const uint4*>(ring + 1 * a.slot_bytes);
   const unsigned char* Vs = ring + 2 * a.slot_bytes;
-  float S[4][4];
-  wait_stage(1);
-#pragma unroll
-  for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) S[nt][u] = 0.f;
-    const int row = 16 * warp + 8 * nt + g;
-    uint32_t kl[4], kh[4];
-    lds_kfrag(Ks + row * 8, t, i0 - 16 + row, kl, kh);
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-      mma16816(S[nt], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
-  }
-  release_stage(1);
-  // mask: query row rr = g + 8h, key column c = 8nt + 2t + e  ->  distance rr + 16 - c
-  float m[2], lw[2], lr[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int c = 8 * nt + 2 * t + e;
-        const int dist = g + 8 * h + 16 - c;
-        const bool ok = dist >= 0 && dist < W && q0 - 16 + c >= 0;
-        float& s = S[nt][2 * h + e];
-        s = ok ? s : -INFINITY;
-        mx = fmaxf(mx, s);
-      }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    m[h] = mx;  // finite: distance 0 (the query itself) is always in the block
-    float sum = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float& s = S[nt][2 * h + e];
-        s = exp2f(s - mx);
-        sum += s;
-      }
-    lw[h] = sum;  // lane-partial window sum
-    lr[h] = 0.f;  // rung sum (nonzero in the holder lane of the quad only)
-  }
-  // ---- window: O = P V'.  ldmatrix lane l supplies row (l&7) of matrix l>>3: keys
-  // 16 s2 + 8 ((l>>3)&1) + (l&7), chunk nd + (l>>4).  Rows outside [w0, i_last] (P = 0 there)
-  // are read from the nearest copied row, so that no stale value can turn 0 * x into NaN.
-  float O[8][4];  // [n-tile nt]: (row g: dims 8nt+2t, +1), (row g+8: the same dims)
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) O[nt][0] = O[nt][1] = O[nt][2] = O[nt][3] = 0.f;
+  constexpr int kWin = kNear - 16;  // index of the window block's first row (position i0 - 16)
   const int mi = lane >> 3, rl = lane & 7;
-  wait_stage(2);
-#pragma unroll
-  for (int s2 = 0; s2 < 2; ++s2) {
-    const uint32_t pa0 = pack_h2(S[2 * s2][0], S[2 * s2][1]);
-    const uint32_t pa1 = pack_h2(S[2 * s2][2], S[2 * s2][3]);
-    const uint32_t pa2 = pack_h2(S[2 * s2 + 1][0], S[2 * s2 + 1][1]);
-    const uint32_t pa3 = pack_h2(S[2 * s2 + 1][2], S[2 * s2 + 1][3]);
-    const int pc = min(max(q0 - 16 + 16 * s2 + (mi & 1) * 8 + rl, w0), i_last);
-    const unsigned char* vrow = Vs + (pc - (i0 - 16)) * kRowBytes;
-    const int sw = swz(pc);
-#pragma unroll
-    for (int nd = 0; nd < 8; nd += 2) {
-      uint32_t b[4];
-      ldsm_x4_trans(b, vrow + ((nd + (mi >> 1)) ^ sw) * 16);
-      mma16816(O[nd], pa0, pa1, pa2, pa3, b[0], b[1]);
-      mma16816(O[nd + 1], pa0, pa1, pa2, pa3, b[2], b[3]);
-    }
-  }
-  release_stage(2);
-
-  // ---- rungs: one per online-softmax step; rung r is stage 3 + r.
-  // Slab row of query i: i - i0 + kI (global row i - lo; interp: its partner i - lo - 1 is
-  // the row before).  Rows that a query does not attend are read from the slab's first
-  // copied row (finite data) and get p = 0; a warp none of whose rows attends a rung skips
-  // it as a whole (a uniform branch).
+  // Rung layout.  Slab row of query i: i - i0 + kI (global row i - lo; interp: its partner
+  // i - lo - 1 is the row before).  Rows that a query does not attend are read from the slab's
+  // first copied row (finite data) and get p = 0; a warp none of whose rows attends a rung
+  // skips it as a whole (a uniform branch).
   // Diagonal: query g's score sits in lane (g, g>>1) of key n-tile 0, element g&1; query
   // g+8's in the same lane of n-tile 1, element 2 + (g&1).  Only that "holder" lane keeps a
   // rung's score (the other three take -inf, so p = 0 there), and it holds the nonzero
@@ -387,13 +329,9 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   int srow[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) srow[h] = ic[h] - i0 + kI;
-  // ring slot and phase parity of the current stage (stage 3 + r sits in slot (3 + r) %
-  // kSlots, phase (3 + r) / kSlots), advanced as the loop runs
-  int slot = 3 % kSlots;
-  uint32_t par = (3 / kSlots) & 1;
   const int vbase = 16 * warp + (mi & 1) * 8 + rl + kI;  // ldmatrix row of this lane, before clamping
-  // A rung's metadata does not depend on the staged rows: it is computed for the next rung
-  // while the current rung's products are in flight.
+  // A rung's metadata does not depend on the staged rows (it is computed for the next
+  // streamed rung while the current one's products are in flight).
   int first = 0, fcop = 0, rowu[2] = {0, 0};
   bool ok[2] = {false, false}, act = false;
   float wr = 0.f;
@@ -411,55 +349,183 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
     act = __any_sync(0xffffffffu, ok[0] || ok[1]);
     if (MODE == 1) wr = ks.w[c];
   };
-  if (nrt > 0) meta(0);
-  for (int r = 0; r < nrt; ++r) {
+  // The rung's diagonal scores (holder lanes; -inf elsewhere) from the K' rows at kst (slab
+  // row 0), for the current metadata.
+  auto rung_scores = [&](const uint4* kst, float (&sc)[2]) {
+    float d[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t kl[4], kh[4];
+      lds_kfrag(kst + rowu[h] * 8, t, first + rowu[h], kl, kh);
+      if (MODE == 0) {
+        // two independent halves of the k-sum: MMA dependency chains of two, not four
+        float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(ca, qa[0][0][0], qa[1][0][0], qa[0][1][0], qa[1][1][0], kl[0], kh[0]);
+        mma16816(cb, qa[0][0][2], qa[1][0][2], qa[0][1][2], qa[1][1][2], kl[2], kh[2]);
+        mma16816(ca, qa[0][0][1], qa[1][0][1], qa[0][1][1], qa[1][1][1], kl[1], kh[1]);
+        mma16816(cb, qa[0][0][3], qa[1][0][3], qa[0][1][3], qa[1][1][3], kl[3], kh[3]);
+        d[h] = (g & 1) ? ca[2 * h + 1] + cb[2 * h + 1] : ca[2 * h] + cb[2 * h];
+      } else {  // (interp keeps registers for its second row)
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          mma16816(c, qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
+        d[h] = (g & 1) ? c[2 * h + 1] : c[2 * h];
+      }
+    }
+    if (MODE == 1 && wr > 0.f) {  // uniform: w belongs to the rung
+      float C2[2][4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = max(rowu[h] - 1, fcop);
+        uint32_t kl[4], kh[4];
+        lds_kfrag(kst + row * 8, t, first + row, kl, kh);
+        C2[h][0] = C2[h][1] = C2[h][2] = C2[h][3] = 0.f;
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          mma16816(C2[h], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
+      }
+      d[0] = (1.f - wr) * d[0] + wr * ((g & 1) ? C2[0][1] : C2[0][0]);
+      d[1] = (1.f - wr) * d[1] + wr * ((g & 1) ? C2[1][3] : C2[1][2]);
+    }
+    sc[0] = holder && ok[0] ? d[0] : -INFINITY;
+    sc[1] = holder && ok[1] ? d[1] : -INFINITY;
+  };
+  // O += diag(p (1-w)) V'[slab rows of the 16 queries]; interp: + diag(p w) V'[rows - 1], the
+  // V' rows at vst (slab row 0), for the current metadata.
+  auto rung_pv = [&](const unsigned char* vst, const float (&p)[2], float (&O)[8][4]) {
+#pragma unroll
+    for (int part = 0; part < (MODE == 1 ? 2 : 1); ++part) {
+      if (part == 1 && !(wr > 0.f)) break;  // uniform
+      const float f = MODE == 1 ? (part == 0 ? 1.f - wr : wr) : 1.f;
+      const float x0 = p[0] * f, x1 = p[1] * f;
+      const uint32_t a0 = (g & 1) ? pack_h2(0.f, x0) : pack_h2(x0, 0.f);
+      const uint32_t a3 = (g & 1) ? pack_h2(0.f, x1) : pack_h2(x1, 0.f);
+      const int vr = min(max(vbase - part, fcop), lcop);
+      const unsigned char* vrow = vst + vr * kRowBytes;
+      const int sw = swz(first + vr);
+#pragma unroll
+      for (int nd = 0; nd < 8; nd += 2) {
+        uint32_t b[4];
+        ldsm_x4_trans(b, vrow + ((nd + (mi >> 1)) ^ sw) * 16);
+        mma16816(O[nd], a0, 0u, 0u, a3, b[0], b[1]);
+        mma16816(O[nd + 1], a0, 0u, 0u, a3, b[2], b[3]);
+      }
+    }
+  };
+
+  // ---- window band S = Q' K'^T over keys [q0-16, q0+16), and the near rungs' scores
+  float S[4][4];
+  float pn[kMaxNear][2];  // near rungs: scores, then probabilities
+  wait_stage(1);
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) S[nt][u] = 0.f;
+    const int row = 16 * warp + 8 * nt + g;
+    uint32_t kl[4], kh[4];
+    lds_kfrag(Ks + (kWin + row) * 8, t, i0 - 16 + row, kl, kh);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      mma16816(S[nt], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxNear; ++j) {
+    pn[j][0] = pn[j][1] = -INFINITY;
+    if (j < n_near) {  // uniform
+      meta(j);
+      if (act) rung_scores(Ks + (first - (i0 - kNear)) * 8, pn[j]);  // uniform
+    }
+  }
+  release_stage(1);
+  // mask: query row rr = g + 8h, key column c = 8nt + 2t + e  ->  distance rr + 16 - c.  The
+  // reference m is the exact maximum over the window band and the near rungs.
+  float m[2], lw[2], lr[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int c = 8 * nt + 2 * t + e;
+        const int dist = g + 8 * h + 16 - c;
+        const bool ok = dist >= 0 && dist < W && q0 - 16 + c >= 0;
+        float& s = S[nt][2 * h + e];
+        s = ok ? s : -INFINITY;
+        mx = fmaxf(mx, s);
+      }
+#pragma unroll
+    for (int j = 0; j < kMaxNear; ++j) mx = fmaxf(mx, pn[j][h]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    m[h] = mx;  // finite: distance 0 (the query itself) is always in the block
+    float sum = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float& s = S[nt][2 * h + e];
+        s = exp2f(s - mx);
+        sum += s;
+      }
+    lw[h] = sum;  // lane-partial window sum
+    float rs = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxNear; ++j) {
+      pn[j][h] = exp2f(pn[j][h] - mx);  // 0 outside the holder lanes and for absent rungs
+      rs += pn[j][h];
+    }
+    lr[h] = rs;  // rung sum (nonzero in the holder lane of the quad only)
+  }
+  // ---- O = P V' over the window band, then the near rungs.  Window: ldmatrix lane l supplies
+  // row (l&7) of matrix l>>3: keys 16 s2 + 8 ((l>>3)&1) + (l&7), chunk nd + (l>>4).  Rows
+  // outside [w0, i_last] (P = 0 there) are read from the nearest copied row, so that no stale
+  // value can turn 0 * x into NaN.
+  float O[8][4];  // [n-tile nt]: (row g: dims 8nt+2t, +1), (row g+8: the same dims)
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) O[nt][0] = O[nt][1] = O[nt][2] = O[nt][3] = 0.f;
+  wait_stage(2);
+#pragma unroll
+  for (int s2 = 0; s2 < 2; ++s2) {
+    const uint32_t pa0 = pack_h2(S[2 * s2][0], S[2 * s2][1]);
+    const uint32_t pa1 = pack_h2(S[2 * s2][2], S[2 * s2][3]);
+    const uint32_t pa2 = pack_h2(S[2 * s2 + 1][0], S[2 * s2 + 1][1]);
+    const uint32_t pa3 = pack_h2(S[2 * s2 + 1][2], S[2 * s2 + 1][3]);
+    const int pc = min(max(q0 - 16 + 16 * s2 + (mi & 1) * 8 + rl, w0), i_last);
+    const unsigned char* vrow = Vs + (pc - (i0 - kNear)) * kRowBytes;
+    const int sw = swz(pc);
+#pragma unroll
+    for (int nd = 0; nd < 8; nd += 2) {
+      uint32_t b[4];
+      ldsm_x4_trans(b, vrow + ((nd + (mi >> 1)) ^ sw) * 16);
+      mma16816(O[nd], pa0, pa1, pa2, pa3, b[0], b[1]);
+      mma16816(O[nd + 1], pa0, pa1, pa2, pa3, b[2], b[3]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxNear; ++j) {
+    if (j < n_near) {  // uniform
+      meta(j);
+      if (act) rung_pv(Vs + (first - (i0 - kNear)) * kRowBytes, pn[j], O);  // uniform
+    }
+  }
+  release_stage(2);
+
+  // ---- streamed rungs: one per online-softmax step; rung r is stage 3 + r - n_near.
+  // Ring slot and phase parity of the current stage (stage n sits in slot n % kSlots, phase
+  // n / kSlots), advanced as the loop runs.
+  int slot = 3 % kSlots;
+  uint32_t par = (3 / kSlots) & 1;
+  if (n_near < nrt) meta(n_near);
+  for (int r = n_near; r < nrt; ++r) {
     if (!s_err && !mbar_wait(&full_bar[slot], par, a.wait_ns)) {
       s_err = 1;
       atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
     }
     const unsigned char* st = ring + slot * a.slot_bytes;
     float sc[2] = {-INFINITY, -INFINITY};
-    if (act) {  // uniform
-      const uint4* kst = reinterpret_cast<const uint4*>(st);
-      float d[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t kl[4], kh[4];
-        lds_kfrag(kst + rowu[h] * 8, t, first + rowu[h], kl, kh);
-        if (MODE == 0) {
-          // two independent halves of the k-sum: MMA dependency chains of two, not four
-          float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
-          mma16816(ca, qa[0][0][0], qa[1][0][0], qa[0][1][0], qa[1][1][0], kl[0], kh[0]);
-          mma16816(cb, qa[0][0][2], qa[1][0][2], qa[0][1][2], qa[1][1][2], kl[2], kh[2]);
-          mma16816(ca, qa[0][0][1], qa[1][0][1], qa[0][1][1], qa[1][1][1], kl[1], kh[1]);
-          mma16816(cb, qa[0][0][3], qa[1][0][3], qa[0][1][3], qa[1][1][3], kl[3], kh[3]);
-          d[h] = (g & 1) ? ca[2 * h + 1] + cb[2 * h + 1] : ca[2 * h] + cb[2 * h];
-        } else {  // (interp keeps registers for its second row)
-          float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int s = 0; s < 4; ++s)
-            mma16816(c, qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
-          d[h] = (g & 1) ? c[2 * h + 1] : c[2 * h];
-        }
-      }
-      if (MODE == 1 && wr > 0.f) {  // uniform: w belongs to the rung
-        float C2[2][4];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int row = max(rowu[h] - 1, fcop);
-          uint32_t kl[4], kh[4];
-          lds_kfrag(kst + row * 8, t, first + row, kl, kh);
-          C2[h][0] = C2[h][1] = C2[h][2] = C2[h][3] = 0.f;
-#pragma unroll
-          for (int s = 0; s < 4; ++s)
-            mma16816(C2[h], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
-        }
-        d[0] = (1.f - wr) * d[0] + wr * ((g & 1) ? C2[0][1] : C2[0][0]);
-        d[1] = (1.f - wr) * d[1] + wr * ((g & 1) ? C2[1][3] : C2[1][2]);
-      }
-      sc[0] = holder && ok[0] ? d[0] : -INFINITY;
-      sc[1] = holder && ok[1] ? d[1] : -INFINITY;
-    }
+    if (act) rung_scores(reinterpret_cast<const uint4*>(st), sc);  // uniform
     // Online softmax with a lazy reference: m only moves when a score passes it by more
     // than 8 (log2 units), so p = 2^(s - m) <= 256 (exact in f16 range) and O and the sums
     // are rescaled only then.
@@ -482,32 +548,13 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
       }
     }
     if (act) {  // uniform
-      const unsigned char* vst = st + SR * kRowBytes;
       float p[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         p[h] = exp2f(sc[h] - m[h]);  // 0 outside the holder lanes and for rows that do not attend
         lr[h] += p[h];
       }
-      // O += diag(p (1-w)) V'[slab rows of the 16 queries]; interp: + diag(p w) V'[rows - 1]
-#pragma unroll
-      for (int part = 0; part < (MODE == 1 ? 2 : 1); ++part) {
-        if (part == 1 && !(wr > 0.f)) break;  // uniform
-        const float f = MODE == 1 ? (part == 0 ? 1.f - wr : wr) : 1.f;
-        const float x0 = p[0] * f, x1 = p[1] * f;
-        const uint32_t a0 = (g & 1) ? pack_h2(0.f, x0) : pack_h2(x0, 0.f);
-        const uint32_t a3 = (g & 1) ? pack_h2(0.f, x1) : pack_h2(x1, 0.f);
-        const int vr = min(max(vbase - part, fcop), lcop);
-        const unsigned char* vrow = vst + vr * kRowBytes;
-        const int sw = swz(first + vr);
-#pragma unroll
-        for (int nd = 0; nd < 8; nd += 2) {
-          uint32_t b[4];
-          ldsm_x4_trans(b, vrow + ((nd + (mi >> 1)) ^ sw) * 16);
-          mma16816(O[nd], a0, 0u, 0u, a3, b[0], b[1]);
-          mma16816(O[nd + 1], a0, 0u, 0u, a3, b[2], b[3]);
-        }
-      }
+      rung_pv(st + SR * kRowBytes, p, O);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[slot]);

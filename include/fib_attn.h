@@ -221,8 +221,9 @@ int fib_attn_debug_indices(fib_attn_plan_t p, int layer, int N, int i_begin, int
  * the bulk-copy engine wait on mbarriers; every such wait gives up after wait_ns
  * nanoseconds (default 1e9; accepted range [1e3, 6e10]), records FIB_ERR_TIMEOUT in the
  * status word, lets the copies already in flight land and returns without writing output.
- * skip_first_rung_copy != 0 makes the bf16 forward never complete its first rung stage, so
- * that a test can drive that timeout path without any device fault.  Host-only; takes
+ * skip_first_rung_copy != 0 makes the bf16 forward never complete one of its staged copies
+ * (the values of the window block), so that a test can drive that timeout path without any
+ * device fault.  Host-only; takes
  * effect on the next launch.  FIB_ERR_INVALID_ARG on a null plan or wait_ns out of range.   */
 int fib_attn_plan_set_debug(fib_attn_plan_t p, int skip_first_rung_copy, long long wait_ns);
 

@@ -412,9 +412,9 @@ def test_prepare_then_attend_equals_the_fused_call(mode):
 
 # ------------------------------------------------------------------ bounded waits
 def test_starved_stage_times_out_and_context_survives():
-    """The hook leaves the first rung stage of every CTA (each attends d = 13) without its copy; each CTA's wait
-    gives up after 2 ms, records FIB_ERR_TIMEOUT and exits.  The same context then runs a
-    normal forward that matches the oracle."""
+    """The hook leaves one staged copy of every CTA (the values of its window block) out; each
+    CTA's wait gives up after 2 ms, records FIB_ERR_TIMEOUT and exits.  The same context then
+    runs a normal forward that matches the oracle."""
     B, H, N, W, alpha = 1, 2, 256, 12, 1.0
     plan = _plan("fib", [alpha], W, N, "mask")
     q, k, v = inputs.qkv(B, H, N, 64, 500, 0, "bf16")
