@@ -13,7 +13,7 @@
 //     shared-memory ring with cp.async.bulk (mbarrier completion): the Q rows, the "near
 //     block" rows [i0-64, i0+64) of K' and of V', then per remaining rung the slab rows
 //     [i0-d, i0-d+64) of K' and V'.  The near block holds the window band and the slab of
-//     every rung with d <= 64 (up to 5 or 6 of them), so those rungs need no copy of their
+//     every rung with d <= 64 (up to 5, interp 4, of them), so those rungs need no copy of their
 //     own and are computed together with the window.  The producer refills a slot once the
 //     4 compute warps release it; with one streamed rung per online-softmax step the next
 //     two stages are in flight while a rung is being computed.  The producer issues the Q
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   // Rungs whose slab lies inside the near block (ascending distances: a prefix) are served
   // from it, up to kMaxNear of them (per path, the largest count whose score registers fit
   // the 96-register budget without spilling); every other rung streams its own slab.
-  constexpr int kMaxNear = MODE == 0 ? 5 : 6;
+  constexpr int kMaxNear = MODE == 0 ? 5 : 4;
   const int n_near = min(kMaxNear, __popc(__ballot_sync(0xffffffffu, lane < nrt && ks.lo[W + lane] + kI <= kNear)));
   const int n_stages = 3 + nrt - n_near;  // Q, near K', near V', then one per streamed rung
 
@@ -353,11 +353,11 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   // row 0), for the current metadata.
   auto rung_scores = [&](const uint4* kst, float (&sc)[2]) {
     float d[2];
+    if (MODE == 0) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t kl[4], kh[4];
-      lds_kfrag(kst + rowu[h] * 8, t, first + rowu[h], kl, kh);
-      if (MODE == 0) {
+      for (int h = 0; h < 2; ++h) {
+        uint32_t kl[4], kh[4];
+        lds_kfrag(kst + rowu[h] * 8, t, first + rowu[h], kl, kh);
         // two independent halves of the k-sum: MMA dependency chains of two, not four
         float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
         mma16816(ca, qa[0][0][0], qa[1][0][0], qa[0][1][0], qa[1][1][0], kl[0], kh[0]);
@@ -365,28 +365,38 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
         mma16816(ca, qa[0][0][1], qa[1][0][1], qa[0][1][1], qa[1][1][1], kl[1], kh[1]);
         mma16816(cb, qa[0][0][3], qa[1][0][3], qa[0][1][3], qa[1][1][3], kl[3], kh[3]);
         d[h] = (g & 1) ? ca[2 * h + 1] + cb[2 * h + 1] : ca[2 * h] + cb[2 * h];
-      } else {  // (interp keeps registers for its second row)
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          mma16816(c, qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
-        d[h] = (g & 1) ? c[2 * h + 1] : c[2 * h];
       }
-    }
-    if (MODE == 1 && wr > 0.f) {  // uniform: w belongs to the rung
-      float C2[2][4];
+    } else {
+      // Interp, banded: column g of key n-tile nt holds slab row R0 + 8nt + g, R0 = 16 warp +
+      // kI - 8, so that the row of query g + 8h is column g of n-tile h + 1 and its partner
+      // (the row before) column (g + 7) & 7 of n-tile h + (g + 7) / 8: 12 MMAs give both
+      // diagonals.  Rows outside [fcop, lcop] are read from the nearest copied row; no
+      // attending query picks those columns.
+      const int R0 = 16 * warp + kI - 8;
+      float C[3][4];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int row = max(rowu[h] - 1, fcop);
+      for (int nt = 0; nt < 3; ++nt) {
+        const int row = min(max(R0 + 8 * nt + g, fcop), lcop);
         uint32_t kl[4], kh[4];
         lds_kfrag(kst + row * 8, t, first + row, kl, kh);
-        C2[h][0] = C2[h][1] = C2[h][2] = C2[h][3] = 0.f;
+        C[nt][0] = C[nt][1] = C[nt][2] = C[nt][3] = 0.f;
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          mma16816(C2[h], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
+          mma16816(C[nt], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], kl[s], kh[s]);
       }
-      d[0] = (1.f - wr) * d[0] + wr * ((g & 1) ? C2[0][1] : C2[0][0]);
-      d[1] = (1.f - wr) * d[1] + wr * ((g & 1) ? C2[1][3] : C2[1][2]);
+      d[0] = (g & 1) ? C[1][1] : C[1][0];  // the holder lane's diagonal entries
+      d[1] = (g & 1) ? C[2][3] : C[2][2];
+      if (wr > 0.f) {  // uniform: w belongs to the rung
+        // the partner entry sits in lane (g, pc >> 1) of the quad: fetch it from there
+        const int pc = (g + 7) & 7;
+        const bool lo_tile = g == 0;  // column 7 of the n-tile before
+        float v0 = lo_tile ? ((pc & 1) ? C[0][1] : C[0][0]) : ((pc & 1) ? C[1][1] : C[1][0]);
+        float v1 = lo_tile ? ((pc & 1) ? C[1][3] : C[1][2]) : ((pc & 1) ? C[2][3] : C[2][2]);
+        v0 = __shfl_sync(0xffffffffu, v0, 4 * g + (pc >> 1));
+        v1 = __shfl_sync(0xffffffffu, v1, 4 * g + (pc >> 1));
+        d[0] = (1.f - wr) * d[0] + wr * v0;
+        d[1] = (1.f - wr) * d[1] + wr * v1;
+      }
     }
     sc[0] = holder && ok[0] ? d[0] : -INFINITY;
     sc[1] = holder && ok[1] ? d[1] : -INFINITY;
