@@ -385,14 +385,14 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
     if (__any_sync(0xffffffffu, ok[0] || ok[1])) {
       const uint4* kst = reinterpret_cast<const uint4*>(slot_of(n));
       const uint4* vst = reinterpret_cast<const uint4*>(slot_of(n) + SR * kRowBytes);
-      // scores and dP of the row (slab row rowu) and, interp, of its partner (rowu - 1)
+      // scores and dP of the row (slab row rowu) and, interp, of its partner (rowu - 1),
+      // broadcast to the row's quad
       float sc[2][2], dp[2][2];  // [part][h]
-#pragma unroll
-      for (int part = 0; part < (MODE == 1 ? 2 : 1); ++part) {
+      if (MODE == 0) {
         float C[2][4], E[2][4];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int row = part == 0 ? rowu[h] : max(rowu[h] - 1, fcop);
+          const int row = rowu[h];
           uint32_t kl[4], kh[4], vl[4], vh[4];
           lds_kfrag(kst + row * 8, t, first + row, kl, kh);
           lds_kfrag(vst + row * 8, t, first + row, vl, vh);
@@ -404,10 +404,46 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
             mma16816(E[h], da[0][0][s], da[1][0][s], da[0][1][s], da[1][1][s], vl[s], vh[s]);
           }
         }
-        sc[part][0] = __shfl_sync(0xffffffffu, (g & 1) ? C[0][1] : C[0][0], src_lane);
-        sc[part][1] = __shfl_sync(0xffffffffu, (g & 1) ? C[1][3] : C[1][2], src_lane);
-        dp[part][0] = __shfl_sync(0xffffffffu, (g & 1) ? E[0][1] : E[0][0], src_lane);
-        dp[part][1] = __shfl_sync(0xffffffffu, (g & 1) ? E[1][3] : E[1][2], src_lane);
+        sc[0][0] = __shfl_sync(0xffffffffu, (g & 1) ? C[0][1] : C[0][0], src_lane);
+        sc[0][1] = __shfl_sync(0xffffffffu, (g & 1) ? C[1][3] : C[1][2], src_lane);
+        dp[0][0] = __shfl_sync(0xffffffffu, (g & 1) ? E[0][1] : E[0][0], src_lane);
+        dp[0][1] = __shfl_sync(0xffffffffu, (g & 1) ? E[1][3] : E[1][2], src_lane);
+      } else {
+        // Banded, as in the forward: column g of key n-tile nt holds slab row R0 + 8nt + g,
+        // R0 = 16 warp + kI - 8, so the row of query g + 8h is column g of n-tile h + 1 and its
+        // partner column (g + 7) & 7 of n-tile h + (g + 7) / 8: 12 MMAs for both diagonals of
+        // S, 12 for dP.  Rows outside [fcop, lcop] are read from the nearest copied row; no
+        // attending query picks those columns.
+        const int R0 = 16 * warp + kI - 8;
+        const int pc = (g + 7) & 7;
+        const int plane = 4 * g + (pc >> 1);  // lane holding the partner entries of rows g, g+8
+        const bool lo_tile = g == 0;          // partner in column 7 of the n-tile before
+#pragma unroll
+        for (int op = 0; op < 2; ++op) {  // 0: S from K', 1: dP from V'
+          const uint4* bst = op == 0 ? kst : vst;
+          float C[3][4];
+#pragma unroll
+          for (int nt = 0; nt < 3; ++nt) {
+            const int row = min(max(R0 + 8 * nt + g, fcop), lcop);
+            uint32_t bl[4], bh[4];
+            lds_kfrag(bst + row * 8, t, first + row, bl, bh);
+            C[nt][0] = C[nt][1] = C[nt][2] = C[nt][3] = 0.f;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              if (op == 0)
+                mma16816(C[nt], qa[0][0][s], qa[1][0][s], qa[0][1][s], qa[1][1][s], bl[s], bh[s]);
+              else
+                mma16816(C[nt], da[0][0][s], da[1][0][s], da[0][1][s], da[1][1][s], bl[s], bh[s]);
+            }
+          }
+          float (&out)[2][2] = op == 0 ? sc : dp;
+          out[0][0] = __shfl_sync(0xffffffffu, (g & 1) ? C[1][1] : C[1][0], src_lane);
+          out[0][1] = __shfl_sync(0xffffffffu, (g & 1) ? C[2][3] : C[2][2], src_lane);
+          const float v0 = lo_tile ? ((pc & 1) ? C[0][1] : C[0][0]) : ((pc & 1) ? C[1][1] : C[1][0]);
+          const float v1 = lo_tile ? ((pc & 1) ? C[1][3] : C[1][2]) : ((pc & 1) ? C[2][3] : C[2][2]);
+          out[1][0] = __shfl_sync(0xffffffffu, v0, plane);
+          out[1][1] = __shfl_sync(0xffffffffu, v1, plane);
+        }
       }
       float ds[2];
 #pragma unroll
