@@ -122,8 +122,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        const float2* __restrict__ lo_tab,
                                                        const float2* __restrict__ hi_tab, int N, long long rows,
                                                        float qscale) {
-  // The dependent dQ grid may launch at once (its CTAs take the SMs as this single wave
-  // drains); it waits for the whole of this grid before it reads what this grid writes.
+  // The dependent dQ grid may launch at once (its CTAs take the SMs as this grid drains);
+  // it waits for the whole of this grid before it reads what this grid writes.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const long long gid = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
   const long long row = gid >> 2;
@@ -667,15 +667,12 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
   // of query i: i - (j0 + lo).  dk' += diag(wt dS) Q's[slab], dv += diag(wt P) dO'[slab].
   const float sel_lo = (t == (g >> 1) && !(g & 1)) ? 1.f : 0.f;
   const float sel_hi = (t == (g >> 1) && (g & 1)) ? 1.f : 0.f;
-  for (int r = 0; r < nrk; ++r) {
-    const int n = 1 + r;
+  // stored (P, dS) of the query of key k0 + g + 8h for each role: loaded one rung ahead, so
+  // that their latency overlaps the previous rung's products
+  auto load_pds = [&](int r, float2 (&v)[2][2]) {
     const int c = W + r;
     const int lo = ks.lo[c];
-    const float w = MODE == 1 ? ks.w[c] : 0.f;
     const int need = ks.need[c];
-    const int qfirst = j0 + lo;
-    const int xlast = min(qfirst + kBTileT, N - 1) - qfirst;  // last copied slab row
-    float2 v[2][2];  // [role][h]: stored (P, dS) of the query of key k0 + g + 8h
 #pragma unroll
     for (int role = 0; role < 2; ++role)
 #pragma unroll
@@ -684,6 +681,22 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
         const bool ok = (role == 0 || MODE == 1) && k0 + g + 8 * h <= j_last && i < N && i >= need;
         v[role][h] = ok ? __ldg(pds + static_cast<size_t>(i) * stride + c) : make_float2(0.f, 0.f);
       }
+  };
+  float2 vn[2][2];
+  if (nrk > 0) load_pds(0, vn);
+  for (int r = 0; r < nrk; ++r) {
+    const int n = 1 + r;
+    const int c = W + r;
+    const int lo = ks.lo[c];
+    const float w = MODE == 1 ? ks.w[c] : 0.f;
+    const int qfirst = j0 + lo;
+    const int xlast = min(qfirst + kBTileT, N - 1) - qfirst;  // last copied slab row
+    float2 v[2][2];  // [role][h]
+#pragma unroll
+    for (int role = 0; role < 2; ++role)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) v[role][h] = vn[role][h];
+    if (r + 1 < nrk) load_pds(r + 1, vn);
     wait_stage(n);
     const unsigned char* qst = slot_of(n);
 #pragma unroll

@@ -88,10 +88,6 @@ struct TcArgs {
   int skip_first_rung_copy;    // test hook: never arrive on rung 0's stage
 };
 
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;\n" ::"n"(kConsumers) : "memory");
-}
-
 // ------------------------------------------------------------------ K', V' preparation
 // One thread per (row, quarter u): frequencies m = 8u .. 8u+7, i.e. chunks u (dims 8u..) and
 // u+4 (their rotate-half partners 32+8u..) of the K row, and the same two chunks of V.
@@ -101,9 +97,9 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const __nv_bfloat16* __res
                                                       const float2* __restrict__ lo_tab,
                                                       const float2* __restrict__ hi_tab, int N,
                                                       long long rows) {
-  // The dependent attention grid may launch at once: its CTAs take the SMs as this single
-  // wave drains and load and rotate their Q rows meanwhile; each waits for the whole of this
-  // grid (griddepcontrol.wait) before it reads K'/V'.
+  // The dependent attention grid may launch at once: its CTAs take the SMs as this grid
+  // drains and load and rotate their Q rows meanwhile; each waits for the whole of this grid
+  // (griddepcontrol.wait) before it reads K'/V'.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const long long gid = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
   const long long row = gid >> 2;
