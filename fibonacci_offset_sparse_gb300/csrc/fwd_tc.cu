@@ -65,8 +65,12 @@ constexpr int kTcMaxW = 16;
 #define FIB_TC_MIN_CTAS_INTERP 4
 #endif
 constexpr int kSlots = FIB_TC_SLOTS;           // ring slots
-constexpr int kNear = 64;     // the near block holds K'/V' rows [i0 - kNear, i0 + 64)
-
+constexpr int kNear = 64;     // the near block holds K'/V' rows [i0 - kNear, i0 + kTcTile)
+// Q, the near K' and the near V' are in flight at once, and a near block fills one slot
+// (a slot holds 2 * kTcTile rows, interp 2 * (kTcTile + 1)).
+static_assert(kSlots >= 3, "the first three stages need their own slots");
+static_assert(kNear <= kTcTile, "the near block must fit a ring slot");
+static_assert(kTcWarps >= 1 && kTcWarps <= 8, "compute warps per CTA");
 
 struct TcArgs {
   LayerTable t;
