@@ -13,25 +13,26 @@
 //     shared-memory ring with cp.async.bulk (mbarrier completion): the Q rows, the "near
 //     block" rows [i0-64, i0+64) of K' and of V', then per remaining rung the slab rows
 //     [i0-d, i0-d+64) of K' and V'.  The near block holds the window band and the slab of
-//     every rung with d <= 64 (up to 5, interp 4, of them), so those rungs need no copy of their
-//     own and are computed together with the window.  The producer refills a slot once the
-//     4 compute warps release it; with one streamed rung per online-softmax step the next
-//     two stages are in flight while a rung is being computed.  The producer issues the Q
-//     copy before the block barrier.  3 slots of 16 KB and 96 registers a thread let 4 CTAs
-//     share an SM.  Every
-//     mbarrier wait is bounded in time; a wait that gives up records FIB_ERR_TIMEOUT in the
-//     plan's status word, the warps stop, and the producer lets its copies in flight land
-//     before the CTA exits.
+//     every rung with d <= 64 (up to 5, interp 4, of them), so those rungs need no copy of
+//     their own and are computed together with the window.  The producer refills a slot
+//     once the 4 compute warps release it; with one streamed rung per online-softmax step
+//     the next two stages are in flight while a rung is being computed.  The producer
+//     issues the Q copy before the block barrier.  3 slots of 16 KB and 96 registers a
+//     thread let 4 CTAs share an SM.  Every mbarrier wait is bounded in time; a wait that
+//     gives up records FIB_ERR_TIMEOUT in the plan's status word, the warps stop, and the
+//     producer lets its copies in flight land before the CTA exits.
 //   * window band: for a warp's 16 queries every window key lies in the 32-row block
 //     [q0-16, q0+16) (W <= 16): S = Q' K'^T and O = P V' as mma.sync m16n8k16 (f16
 //     operands, f32 accumulation), Q' rotated at its own position and scaled by
 //     log2(e)/sqrt(D) so that scores are in log2 units.
 //   * rungs: query i reads slab row i - i0 (+1 for interp), so a rung is the diagonal of a
 //     16x16 block: S_r = diag(Q' K'_slab^T) takes 8 MMAs (2 key n-tiles x 4 k-steps) whose
-//     diagonal is picked out, and O += diag(P) V'_slab takes 8 more (A = diag(P) in f16).
-//     The tensor pipe does 16x the needed products, but it replaces ~250 CUDA-core
-//     instructions per warp and rung (RoPE of the query, bf16 unpacking, dot products,
-//     axpys) with ~40.
+//     diagonal entries sit in one "holder" lane per row, and O += diag(P) V'_slab takes 8
+//     more (A = diag(P) in f16).  Interp reads a 24-row band instead, whose two adjacent
+//     diagonals are the row and its partner (12 MMAs).  The tensor pipe does 16x the needed
+//     products, but a warp-rung costs those MMAs and about a hundred other instructions
+//     where the CUDA cores would need ~250 (RoPE of the query, bf16 unpacking, dot
+//     products, axpys).
 // Register layout: lane (g = lane/4, t = lane%4) owns query rows g and g+8 of its warp.  For
 // the score MMAs the k-order is permuted so that a lane's A fragments hold the dims
 // D_t = [8t, 8t+8) u [32+8t, 32+8t+8) (RoPE partners in the same lane) and its B fragments
@@ -191,8 +192,8 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   const unsigned attended = __ballot_sync(0xffffffffu, lane < nr && ks.need[W + lane] <= i_last);
   const int nrt = 32 - __clz(static_cast<int>(attended));
   // Rungs whose slab lies inside the near block (ascending distances: a prefix) are served
-  // from it, up to kMaxNear of them (per path, the largest count whose score registers fit
-  // the 96-register budget without spilling); every other rung streams its own slab.
+  // from it, up to kMaxNear of them (per path, set by measurement: each near rung holds its
+  // scores in registers until the window's P.V); every other rung streams its own slab.
   constexpr int kMaxNear = MODE == 0 ? 5 : 4;
   const int n_near = min(kMaxNear, __popc(__ballot_sync(0xffffffffu, lane < nrt && ks.lo[W + lane] + kI <= kNear)));
   const int n_stages = 3 + nrt - n_near;  // Q, near K', near V', then one per streamed rung
