@@ -14,13 +14,15 @@
 //     with the chunk swizzle of fwd_tc.cu, and Delta (float32), each row read once.
 //   * bwd_q_kernel (query-owned, 64 queries a CTA): the forward's structure, with dP =
 //     dO'.V'^T beside S = Q's.K'^T and dq' += dS K' in place of O += P V'.  Rungs are
-//     diagonals of 16x16 blocks, as in the forward.  It also writes P and dS of every
-//     attended (query, key slot) -- W + R float pairs a query, the sparse pattern makes
-//     that small -- and each CTA's dalpha partial.
+//     diagonals of 16x16 blocks, as in the forward (interp: one 24-row band per operand
+//     gives the row and its partner).  It also writes P and dS of every attended (query,
+//     key slot) -- W + R float pairs a query, the sparse pattern makes that small -- and
+//     each CTA's dalpha partial.
 //   * bwd_kv_kernel (key-owned, 64 keys a CTA, no atomics): a gather, no score is
 //     recomputed.  The queries that read the CTA's keys stream through a ring (the 80-row
 //     block [j0, j0+80) of Q's and dO' for the window band, then per rung the query slab
-//     [j0+lo, j0+lo+65)); with their stored P and dS, dk' += dS^T Q's and dv += P^T dO'.
+//     [j0+lo, j0+lo+65)); with their stored P and dS (loaded one rung ahead), dk' += dS^T
+//     Q's and dv += P^T dO'.
 //     Its CTA 0 also sums the dQ grid's dalpha partials in a fixed order.
 // Precision as the forward: f16 operands (Q's, K', V', dO', P, dS), f32 accumulation.
 #include <algorithm>
