@@ -365,6 +365,8 @@ def test_device_error_paths():
     (333, 8, 1.2345, "pow2"),
     (150, 4, 1.0, (37,)),
     (1000, 12, 1.4999, "fib"),      # rungs reaching across several 64-query tiles
+    (300, 1, 1.37, tuple(range(1, 25))),  # 24 rungs within 33 rows: more than the near
+                                          # block serves, the rest streamed
 ])
 def test_edge_cases_bf16(mode, N, W, alpha, kind):
     B, H = 2, 3
