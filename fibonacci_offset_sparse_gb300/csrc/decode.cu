@@ -49,7 +49,7 @@ __device__ __forceinline__ float rel_dot_reg(const float (&q)[16], const float (
 }
 
 template <typename DT>
-__global__ void __launch_bounds__(kDecThreads) decode_kernel(DecArgs a) {
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_constant__ DecArgs a) {
   __shared__ KeySmem ks;
   __shared__ float s_m[kDecQuads], s_l[kDecQuads];
   __shared__ float s_o[kDecQuads][kD];
@@ -62,21 +62,44 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(DecArgs a) {
   const DT* V = static_cast<const DT*>(a.v) + static_cast<size_t>(bh) * a.N * kD;
   float q[16];
   load_part(Q, t, q);  // independent of the key table: in flight during its build
-  build_keys(a.t, a.N, &ks);
-  __syncthreads();
+  // The key table: read from the launch parameters where the distances are known on the
+  // host (every mask layer, and interp with the plan's alpha), so that the cache loads issue
+  // at once; built in shared memory from the device alpha otherwise.
+  const bool host_keys = a.t.mode == 0 || a.t.alpha_dev == nullptr;  // uniform
+  if (!host_keys) {
+    build_keys(a.t, a.N, &ks);
+    __syncthreads();
+  }
+  const int W = a.t.W;
 #pragma unroll
   for (int u = 0; u < 16; ++u) q[u] *= kLog2e / 8.0f;
   float o[16];
 #pragma unroll
   for (int u = 0; u < 16; ++u) o[u] = 0.f;
   float m = -INFINITY, l = 0.f;
-  const int nv = ks.nv;
+  const int nv = host_keys ? W + a.t.n : ks.nv;
   // the same trip count in every quad, so that the quad shuffles stay warp-uniform
   for (int c0 = 0; c0 < nv; c0 += kDecQuads) {
     const int c = c0 + quad;
-    const bool ok = c < nv && i >= ks.need[c];
-    const int lo = ok ? ks.lo[c] : 0;
-    const float w = ok ? ks.w[c] : 0.f;
+    // key c: window key c (c < W) or rung c - W, as build_keys lays the table out
+    int klo = 0, kneed = 0;
+    float kw = 0.f;
+    if (c < nv) {
+      if (!host_keys) {
+        klo = ks.lo[c];
+        kw = ks.w[c];
+        kneed = ks.need[c];
+      } else if (c < W) {
+        klo = kneed = c;
+      } else {
+        klo = a.t.lo[c - W];
+        kw = a.t.mode == 1 ? a.t.w[c - W] : 0.f;
+        kneed = klo + (kw > 0.f ? 1 : 0);
+      }
+    }
+    const bool ok = c < nv && i >= kneed;
+    const int lo = ok ? klo : 0;
+    const float w = ok ? kw : 0.f;
     const bool two = w > 0.f;
     // every load of this key first: factors, K and V rows (and the partner rows)
     float2 e0[8], e1[8];
