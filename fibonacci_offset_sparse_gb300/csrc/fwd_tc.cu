@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(256) prep_kv_kernel(const __nv_bfloat16* __res
 
 // ------------------------------------------------------------------ attention kernel
 template <int MODE>
-__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_TC_MIN_CTAS_INTERP) fwd_tc_kernel(TcArgs a) {
+__global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_TC_MIN_CTAS_INTERP) fwd_tc_kernel(const __grid_constant__ TcArgs a) {
   __shared__ KeySmem ks;
   __shared__ __align__(8) uint64_t full_bar[kSlots];
   __shared__ __align__(8) uint64_t empty_bar[kSlots];
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   const int w0 = max(i0 - 16, 0);                // first copied window row
 
   // The producer lane initialises the mbarriers and issues stage 0 (the Q rows, an input of
-  // this grid) before the block barrier, so that the copy overlaps the key-table build.
+  // this grid) before the block barrier, so that the copy overlaps the prologue.
   if (tid == kConsumers) {
     s_err = 0;
     for (int s = 0; s < kSlots; ++s) {
@@ -181,21 +181,29 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
     mbar_arrive_tx(&full_bar[0], bytes);
     bulk_g2s(ring, Q + static_cast<size_t>(i0) * kD, bytes, &full_bar[0]);
   }
-  build_keys(a.t, N, &ks);
+  // Rung table: the mask path reads it from the launch parameters (its distances are known
+  // on the host), so no thread builds it before the block barrier; the interp path builds it
+  // in shared memory (from the device alpha when the caller passes one).  (Reading the
+  // host-known interp table from the parameters too measured slower.)
+  constexpr bool host_keys = MODE == 0;
+  if (!host_keys) build_keys(a.t, N, &ks);
   __syncthreads();  // the only block-wide barrier: the roles split below
   const int W = a.t.W;
-  const int nr = ks.nr;
+  const int nr = host_keys ? a.t.n : ks.nr;
+  auto rung_lo = [&](int r) { return host_keys ? a.t.lo[r] : ks.lo[W + r]; };
+  auto rung_w = [&](int r) { return MODE == 1 ? (host_keys ? a.t.w[r] : ks.w[W + r]) : 0.f; };
+  auto rung_need = [&](int r) { return host_keys ? rung_lo(r) + (rung_w(r) > 0.f ? 1 : 0) : ks.need[W + r]; };
 
   const int warp = tid >> 5, lane = tid & 31;
   // Rungs are kept in ascending distance; the tile streams rungs [0, nrt), up to the last one
   // that some row of it attends (a later tile attends more).
-  const unsigned attended = __ballot_sync(0xffffffffu, lane < nr && ks.need[W + lane] <= i_last);
+  const unsigned attended = __ballot_sync(0xffffffffu, lane < nr && rung_need(lane) <= i_last);
   const int nrt = 32 - __clz(static_cast<int>(attended));
   // Rungs whose slab lies inside the near block (ascending distances: a prefix) are served
   // from it, up to kMaxNear of them (per path, set by measurement: each near rung holds its
   // scores in registers until the window's P.V); every other rung streams its own slab.
   constexpr int kMaxNear = MODE == 0 ? 5 : 4;
-  const int n_near = min(kMaxNear, __popc(__ballot_sync(0xffffffffu, lane < nrt && ks.lo[W + lane] + kI <= kNear)));
+  const int n_near = min(kMaxNear, __popc(__ballot_sync(0xffffffffu, lane < nrt && rung_lo(lane) + kI <= kNear)));
   const int n_stages = 3 + nrt - n_near;  // Q, near K', near V', then one per streamed rung
 
   // ===================================================================== producer
@@ -225,7 +233,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
                  bytes, &full_bar[slot]);
       } else {  // rung slab: rows [first, first + SR) of K', then of V', where inside [0, N)
         const int r = n_near + n - 3;
-        const int lo = ks.lo[W + r];
+        const int lo = rung_lo(r);
         const int first = i0 - lo - kI;
         const int r0 = max(first, 0);
         const int r1 = i_last - lo + 1;
@@ -337,9 +345,8 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   bool ok[2] = {false, false}, act = false;
   float wr = 0.f;
   auto meta = [&](int r) {
-    const int c = W + r;
-    const int lo = ks.lo[c];
-    const int need = ks.need[c];
+    const int lo = rung_lo(r);
+    const int need = rung_need(r);
     first = i0 - lo - kI;          // global row of slab row 0
     fcop = max(0, lo - i0 + kI);   // first copied slab row (<= lcop: the tile attends r)
 #pragma unroll
@@ -348,7 +355,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
       rowu[h] = ok[h] ? srow[h] : fcop;
     }
     act = __any_sync(0xffffffffu, ok[0] || ok[1]);
-    if (MODE == 1) wr = ks.w[c];
+    if (MODE == 1) wr = rung_w(r);
   };
   // The rung's diagonal scores (holder lanes; -inf elsewhere) from the K' rows at kst (slab
   // row 0), for the current metadata.
