@@ -321,15 +321,3 @@ def _dw_term(ds_scaled, p, qr, dO, dk_rows, dv_rows):
     (through the score) and the blended value along v[i-lo-1] - v[i-lo]."""
     return ds_scaled * np.einsum("...nd,...nd->...n", qr, dk_rows) \
         + p * np.einsum("...nd,...nd->...n", dO, dv_rows)
-
-
-def attend_layers(qs, ks, vs, alphas, base_fn, W: int, mode: str = MODE_MASK,
-                  rope_base: float = 10000.0):
-    """Run `attend` for every layer of a stack (layers are independent attention calls).
-
-    base_fn(N) returns the base list for sequence length N.
-    """
-    outs = []
-    for q, k, v, a in zip(qs, ks, vs, alphas):
-        outs.append(attend(q, k, v, a, base_fn(q.shape[-2]), W, mode, rope_base))
-    return outs
