@@ -49,12 +49,25 @@ BACKWARD = "learned-interp-n1024"  # the training configuration: interpolated pa
 
 
 def alphas_for(w):
+    """Per-layer alpha of a workload for the GPU arm: the library's own schedule planner."""
     if w["sched"] == "linear":
         from fibonacci_offset_sparse_gb300 import fib_attn as fa
         return fa.fib_attn_schedule(fa.FIB_SCHED_LINEAR, w["L"])
     if w["sched"] == "coprime":
         from fibonacci_offset_sparse_gb300 import fib_attn as fa
         return fa.fib_attn_schedule(fa.FIB_SCHED_COPRIME, w["L"], 7)
+    if w["sched"] == "learned":
+        from fibonacci_offset_sparse_gb300 import inputs
+        return list(inputs.learned_alpha(w["L"], w["cfg"]))
+    return [1.5] * w["L"]
+
+
+def oracle_alphas_for(w):
+    """The same alphas for the oracle legs, from the oracle's own schedule (nothing of the
+    library is loaded there)."""
+    import oracle
+    if w["sched"] in ("linear", "coprime"):
+        return oracle.schedule(w["sched"], w["L"])
     if w["sched"] == "learned":
         from fibonacci_offset_sparse_gb300 import inputs
         return list(inputs.learned_alpha(w["L"], w["cfg"]))
@@ -91,8 +104,10 @@ def kernel_source_hash():
 
 
 def ncu_traffic(workload):
-    """DRAM bytes per launch of the forward kernel from the committed ncu summary of this
-    workload, or None when absent or taken on a different kernel source."""
+    """DRAM bytes of one layer's forward from the committed ncu summary of this workload:
+    {"layer": steady-state bytes of both kernels of a layer inside the stack, "attend": the
+    attention kernel's bytes in that capture}, or None when the summary is absent or was taken
+    on a different kernel source."""
     p = os.path.join(ROOT, "profiles", f"fwd_{workload}.md")
     if not os.path.exists(p):
         return None
@@ -104,7 +119,7 @@ def ncu_traffic(workload):
     if vals.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
     try:
-        return float(vals["dram_bytes_per_launch"])
+        return {"layer": float(vals["layer_dram_bytes_steady"]), "attend": float(vals["attend_dram_bytes_steady"])}
     except Exception:
         return None
 
@@ -219,11 +234,17 @@ def setup(w, device):
     adev = None
     if w["mode"] == "interp":
         adev = torch.tensor(alphas, dtype=torch.float32, device=device)
-    # one forward workspace per layer (prepared K/V), so that timing one half alone still
-    # reads every layer's own data
+    # The layer stack reuses one forward workspace (the prepared K/V are scratch that each
+    # layer's attention consumes at once, as in a model); timing one half alone uses one
+    # workspace per layer (`wss`), so that every launch reads its own layer's data.
     need = fa.fib_attn_fwd_workspace_size(plan, w["B"], w["H"], w["N"], dev[0][0].dtype)
     wss = [torch.empty(need, dtype=torch.uint8, device=device) if need else None for _ in dev]
     return plan, host, dev, outs, lses, adev, wss
+
+
+def shared_ws(wss):
+    """The stack's one workspace, repeated per layer."""
+    return [wss[0]] * len(wss)
 
 
 def run_stack(fa, plan, dev, outs, lses, adev, wss):
@@ -280,13 +301,14 @@ def time_device(w, steps, warmup, device, rank, world):
     import torch
     from fibonacci_offset_sparse_gb300 import fib_attn as fa
     plan, host, dev, outs, lses, adev, wss = setup(w, device)
+    ws1 = shared_ws(wss)
     stream = torch.cuda.Stream(device)
     with torch.cuda.stream(stream):
-        run_stack(fa, plan, dev, outs, lses, adev, wss)  # first call outside capture
+        run_stack(fa, plan, dev, outs, lses, adev, ws1)  # first call outside capture
     torch.cuda.synchronize(device)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        run_stack(fa, plan, dev, outs, lses, adev, wss)
+        run_stack(fa, plan, dev, outs, lses, adev, ws1)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(device.index if device.index is not None else 0) as clk:
         for _ in range(warmup):
@@ -335,7 +357,7 @@ def time_device(w, steps, warmup, device, rank, world):
             if not first:
                 stream.wait_event(returned[l])  # the previous step's O of layer l is on the host
             with torch.cuda.stream(stream):
-                fa.fib_attn_fwd(plan, l, *dev[l], o=outs[l], lse=lses[l], alpha_dev=adev, workspace=wss[l])
+                fa.fib_attn_fwd(plan, l, *dev[l], o=outs[l], lse=lses[l], alpha_dev=adev, workspace=ws1[l])
                 computed[l].record(stream)
             with torch.cuda.stream(d2h_stream):
                 d2h_stream.wait_event(computed[l])
@@ -418,6 +440,32 @@ def time_decode(mode, B, H, N, L, steps, warmup, device):
     return ms * 1e3
 
 
+def time_dense_ours(w, device, reps=20):
+    """Dense causal attention with the same RoPE through the library's own dense kernel
+    (fib_attn_dense_fwd: K'/V' preparation + the dense blocked kernel), one layer of the
+    workload's shape: milliseconds per layer, CUDA events on the launching stream."""
+    import torch
+    from fibonacci_offset_sparse_gb300 import fib_attn as fa
+    from fibonacci_offset_sparse_gb300 import inputs
+    plan = fa.fib_attn_plan_create(fa.FIB_BASE_FIBONACCI, [1.0], 1, w["N"], fa.FIB_MODE_MASK)
+    q, k, v = (t.to(device) for t in inputs.qkv(w["B"], w["H"], w["N"], 64, w["cfg"], 0, w["dtype"]))
+    o = torch.empty_like(q)
+    lse = torch.empty(w["B"], w["H"], w["N"], dtype=torch.float32, device=device)
+    need = int(fa.lib().fib_attn_dense_fwd_workspace_size(plan.handle, w["B"], w["H"], w["N"], fa.FIB_DTYPE_BF16))
+    ws = torch.empty(need, dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def one():
+        fa.fib_attn_dense_fwd(plan, q, k, v, o=o, lse=lse, workspace=ws)
+
+    with torch.cuda.stream(stream):
+        one()
+    torch.cuda.synchronize(device)
+    ms = time_graph(torch, stream, device, one, reps, 3)
+    plan.close()
+    return ms
+
+
 def time_dense_sdpa(w, device, reps=20):
     """Dense causal attention on the same shape through PyTorch's fused attention (a library
     kernel, timed only as the dense comparison point): milliseconds per layer."""
@@ -440,11 +488,12 @@ def time_dense_sdpa(w, device, reps=20):
 # ----------------------------------------------------------------------------- CPU oracle
 def time_oracle(w, n_layers_sample, heads=None):
     """Oracle seconds per layer of the workload on a sample of layers and heads (every batch
-    row, the full sequence); returns (seconds per full layer, sample description)."""
+    row, the full sequence); returns (seconds per full layer, sample description, seconds
+    actually measured)."""
     import numpy as np  # noqa: F401
     import oracle
     from fibonacci_offset_sparse_gb300 import inputs
-    alphas = alphas_for(w)
+    alphas = oracle_alphas_for(w)
     base = (lambda N: oracle.fibonacci_base()) if w["base"] == "fib" else oracle.pow2_base
     if heads is None:
         heads = w["H"] if w["N"] <= 4096 else 1
@@ -460,7 +509,7 @@ def time_oracle(w, n_layers_sample, heads=None):
     per_layer = t_total / len(layers) / frac_heads
     desc = (f"oracle forward on {len(layers)} of {w['L']} layers" +
             (f", {heads} of {w['H']} heads" if heads < w["H"] else "") + ", float64 numpy, 1 thread")
-    return per_layer, desc
+    return per_layer, desc, t_total
 
 
 def oracle_tokens_per_s(w, per_layer_s):
@@ -490,23 +539,30 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
+        # One reference step = the oracle's forward of one layer on two of the heads (every
+        # batch row, the whole sequence): a bounded sample of the workload.  ms_per_step is the
+        # time such a step takes; value is the workload's tokens/s at that measured rate (the
+        # work grows linearly in layers and heads).
         sample_heads = min(2, w["H"])
         for _ in range(args.warmup):
             time_oracle(w, 1, sample_heads)
-        vals = []
+        step_s = []
         t0 = time.perf_counter()
         for s in range(args.steps):
-            pl, desc = time_oracle(w, 1, sample_heads)
-            vals.append(pl)
+            pl, desc, measured = time_oracle(w, 1, sample_heads)
+            step_s.append(measured)
         el = time.perf_counter() - t0
-        per_layer = statistics.mean(vals)
+        ms_step = statistics.mean(step_s) * 1e3
+        per_layer = statistics.mean(step_s) * w["H"] / sample_heads
         v = oracle_tokens_per_s(w, per_layer)
+        rcfg = dict(cfg, reference_step=f"oracle forward of 1 of {w['L']} layers on {sample_heads} of {w['H']} "
+                                        f"heads (B={w['B']}, N={w['N']}); value = the {w['L']}-layer stack's "
+                                        "tokens/s at the measured rate")
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_layer * w["L"] * 1e3,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic N(0,1), seeded", "config": cfg,
-                "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                 "sample": desc + f"; each step is one layer, scaled to the {w['L']}-layer stack",
+                "data": "synthetic N(0,1), seeded", "config": rcfg,
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc,
                                  "host_cores_available": len(os.sched_getaffinity(0))},
                 "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 "wall_s": el}
@@ -528,11 +584,13 @@ def main():
     e2e_value = job_value(tokens_step, world, r["ms_e2e_per_step"])
     peak, peak_kind = read_peaks()
     layer_s = r["ms_per_step"] / 1e3 / w["L"]
-    # dominant kernel: the attention launch, timed alone (its algorithmic bytes are the
-    # layer's compulsory bytes: Q and the prepared K, V read once, O written once)
+    # The roofline is taken over a layer's whole forward (K'/V' preparation + attention, the
+    # launches a user's fib_attn_fwd makes), timed inside the step: the layer's compulsory
+    # bytes (Q, K, V read once, O written once) over its time.  The attention kernel timed
+    # alone (it reads the prepared K'/V' instead of K and V) is reported beside it.
     launch_s = r["halves"]["attend_ms"] / 1e3 if r["halves"] else layer_s
     algo = compulsory_bytes(w)
-    achieved = algo / launch_s / 1e9
+    achieved = algo / layer_s / 1e9
     traffic = ncu_traffic(args.workload)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -541,11 +599,20 @@ def main():
         "data": "synthetic: i.i.d. N(0,1) Q/K/V per layer (seeded), shaped like the pages' 60M model",
         "config": cfg,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
+                     "frac": achieved / peak, "traffic": traffic["layer"] if traffic else None,
                      "peak_kind": peak_kind + (" (hbm_gbs, burst copy)" if peak_kind == "measured" else ""),
                      "algorithmic_bytes_per_launch": algo,
-                     "avg_launch_us": launch_s * 1e6,
-                     "kernel": "fwd_tc_kernel (attention, prepared K/V)" if r["halves"] else "fwd_kernel"},
+                     "avg_launch_us": layer_s * 1e6,
+                     "kernel": ("one layer's forward: prep_kv_kernel + fwd_tc_kernel" if r["halves"]
+                                else "one layer's forward: fwd_kernel"),
+                     "traffic_note": "steady-state DRAM bytes of one layer's kernels inside the stack (ncu, "
+                                     "caches not flushed between kernels)",
+                     "attention_kernel": {
+                         "avg_launch_us": launch_s * 1e6, "achieved": algo / launch_s / 1e9,
+                         "frac": algo / launch_s / 1e9 / peak,
+                         "traffic": traffic["attend"] if traffic else None,
+                         "note": "fwd_tc_kernel timed alone; its bytes counted as the layer's compulsory ones "
+                                 "(it reads the prepared K'/V' where the layer reads K and V)"}},
         "layer": {"us_per_layer": layer_s * 1e6,
                   "prepare_us_per_launch": r["halves"]["prepare_ms"] * 1e3 if r["halves"] else None,
                   "attend_us_per_launch": r["halves"]["attend_ms"] * 1e3 if r["halves"] else None,
@@ -569,7 +636,9 @@ def main():
                          "ms_per_step": rs["ms_per_step"], "us_per_layer": ls * 1e6,
                          "attend_us_per_launch": la * 1e6,
                          "prepare_us_per_launch": rs["halves"]["prepare_ms"] * 1e3 if rs["halves"] else None,
-                         "achieved_gbs": ach, "frac": ach / peak,
+                         "achieved_gbs": compulsory_bytes(ws) / ls / 1e9,
+                         "frac": compulsory_bytes(ws) / ls / 1e9 / peak,
+                         "attend_achieved_gbs": ach, "attend_frac": ach / peak,
                          "layer_frac": compulsory_bytes(ws) / ls / 1e9 / peak, "traffic": ncu_traffic(name)}
         line["secondary"] = sec
         wb = WORKLOADS[BACKWARD]
@@ -585,19 +654,23 @@ def main():
                             "compulsory_bytes_per_layer": bb,
                             "achieved_gbs": bb / (rb["us_per_layer"] * 1e-6) / 1e9,
                             "frac": bb / (rb["us_per_layer"] * 1e-6) / 1e9 / peak}
-    try:
-        dense = {}
-        for name in [args.workload] + (SECONDARY if args.workload == DEFAULT and not args.no_secondary else []):
-            ws = WORKLOADS[name]
-            dense[name] = {"ms_per_layer": time_dense_sdpa(ws, device),
-                           "sparse_ms_per_layer": (r["ms_per_step"] if name == args.workload
-                                                   else line["secondary"][name]["ms_per_step"]) / ws["L"]}
-        line["dense_causal_sdpa"] = {"kind": "torch scaled_dot_product_attention, causal, same shape, no RoPE",
-                                     "layers": dense}
-    except Exception as exc:  # the comparison is context only
-        line["dense_causal_sdpa"] = {"unavailable": str(exc)[:200]}
+    dense = {}
+    for name in [args.workload] + (SECONDARY if args.workload == DEFAULT and not args.no_secondary else []):
+        ws = WORKLOADS[name]
+        if ws["mode"] != "mask":
+            continue
+        sparse_ms = (r["ms_per_step"] if name == args.workload else line["secondary"][name]["ms_per_step"]) / ws["L"]
+        ours = time_dense_ours(ws, device)
+        dense[name] = {"ms_per_layer": ours, "sparse_ms_per_layer": sparse_ms, "dense_over_sparse": ours / sparse_ms}
+        try:  # a library kernel on the same shape, context only (it applies no RoPE)
+            dense[name]["torch_sdpa_ms_per_layer_no_rope"] = time_dense_sdpa(ws, device)
+        except Exception as exc:
+            dense[name]["torch_sdpa_ms_per_layer_no_rope"] = f"unavailable: {str(exc)[:120]}"
+    line["dense_causal"] = {"kind": "fib_attn_dense_fwd: dense causal attention with the same RoPE, "
+                                    "K'/V' preparation + the library's dense kernel, one layer",
+                            "layers": dense}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        per_layer, desc = time_oracle(w, 3)
+        per_layer, desc, _ = time_oracle(w, 3)
         line["cpu_baseline"] = {"value": oracle_tokens_per_s(w, per_layer), "unit": UNIT, "cores": 1,
                                 "kind": "oracle", "sample": desc + ", scaled to the full stack",
                                 "host_cores_available": len(os.sched_getaffinity(0))}

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfibattn.so")
 
-SOURCES = ["planner.cpp", "api.cu", "fwd.cu", "fwd_tc.cu", "bwd.cu", "bwd_tc.cu", "decode.cu"]
+SOURCES = ["planner.cpp", "api.cu", "fwd.cu", "fwd_tc.cu", "bwd.cu", "bwd_tc.cu", "decode.cu", "dense.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
               "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

@@ -22,7 +22,7 @@ cudaError_t launch_fwd(const LayerTable& t, int B, int H, int N, int dtype, cons
 bool tc_supported(const LayerTable& t);
 size_t fwd_tc_workspace_bytes(int B, int H, int N);
 cudaError_t launch_prep_kv(int B, int H, int N, const void* k, const void* v, const float2* lo_tab,
-                           const float2* hi_tab, void* workspace, cudaStream_t stream);
+                           const float2* hi_tab, void* workspace, int* status, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* workspace,
                           void* o, float* lse, const float2* lo_tab, const float2* hi_tab, int* status,
                           unsigned long long wait_ns, int skip_first_rung_copy, bool after_prep,
@@ -43,6 +43,9 @@ cudaError_t launch_bwd(const LayerTable& t, int B, int H, int N, int dtype, cons
 cudaError_t launch_decode(const LayerTable& t, int B, int H, int N, int pos, int dtype,
                           const void* q, const void* k, const void* v, void* o, float* lse,
                           const float2* lo_tab, const float2* hi_tab, cudaStream_t stream);
+cudaError_t launch_dense_fwd(int B, int H, int N, const void* q, const void* workspace, void* o, float* lse,
+                             const float2* lo_tab, const float2* hi_tab, int* status, unsigned long long wait_ns,
+                             bool after_prep, cudaStream_t stream);
 cudaError_t noalloc_scratch(void** out);
 size_t noalloc_scratch_bytes();
 }  // namespace fibattn
@@ -60,7 +63,8 @@ struct fib_attn_plan_s {
   float2* d_hi = nullptr;
   int* d_status = nullptr;
   unsigned long long wait_ns = 1000000000ULL;  // bound of every device-side wait (1 s)
-  int skip_first_rung_copy = 0;                // test hook, see fib_attn_plan_set_debug
+  int skip_first_rung_copy = 0;                // test hooks, see fib_attn_plan_set_debug
+  int corrupt_rung_table = 0;
 };
 
 namespace {
@@ -107,6 +111,17 @@ int make_table(const fib_attn_plan_s* p, int layer, int N, const float* alpha_de
   return FIB_OK;
 }
 
+// Test hook of the tensor-core forward only (the one kernel family that checks its rung
+// table on the device): the first rung of a host-built table is moved to distance 0, inside
+// the window.  That row is the query's own, so the corrupted table still addresses only rows
+// of the sequence; the kernel's check rejects it before any rung row is copied.
+void corrupt_for_test(const fib_attn_plan_s* p, LayerTable* t) {
+  if (p->corrupt_rung_table && t->n > 0 && t->alpha_dev == nullptr) {
+    t->lo[0] = 0;
+    t->w[0] = 0.f;
+  }
+}
+
 int check_device(const fib_attn_plan_s* p) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FIB_ERR_CUDA;
@@ -148,6 +163,7 @@ const char* fib_attn_error_string(int code) {
     case FIB_ERR_NOMEM: return "out of memory";
     case FIB_ERR_TIMEOUT: return "device wait timed out";
     case FIB_ERR_DEVICE_ASSERT: return "device-side check failed";
+    case FIB_ERR_RANGE: return "value outside the float16 range of the bf16 tensor-core path";
     default: return "unknown status";
   }
 }
@@ -325,8 +341,9 @@ int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, c
   // bf16 with a window of at most 16 keys: K'/V' preparation plus the tensor-core kernel
   // (fwd_tc.cu); otherwise the CUDA-core kernel (fwd.cu), which also serves float32 exactly.
   if (dtype == FIB_DTYPE_BF16 && tc_supported(t)) {
+    corrupt_for_test(p, &t);
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = launch_prep_kv(B, H, N, k, v, p->d_lo, p->d_hi, workspace, s);
+    const cudaError_t e = launch_prep_kv(B, H, N, k, v, p->d_lo, p->d_hi, workspace, p->d_status, s);
     if (e != cudaSuccess) return cuda_status(e);
     return cuda_status(launch_fwd_tc(t, B, H, N, q, workspace, o, lse, p->d_lo, p->d_hi, p->d_status,
                                      p->wait_ns, p->skip_first_rung_copy, true, s));
@@ -346,7 +363,7 @@ int fib_attn_fwd_prepare_kv(fib_attn_plan_t p, int B, int H, int N, int dtype, c
   if (workspace == k || workspace == v) return FIB_ERR_INVALID_ARG;
   st = check_device(p);
   if (st != FIB_OK) return st;
-  return cuda_status(launch_prep_kv(B, H, N, k, v, p->d_lo, p->d_hi, workspace,
+  return cuda_status(launch_prep_kv(B, H, N, k, v, p->d_lo, p->d_hi, workspace, p->d_status,
                                     static_cast<cudaStream_t>(stream)));
 }
 
@@ -367,9 +384,35 @@ int fib_attn_fwd_attend(fib_attn_plan_t p, int layer, int B, int H, int N, int d
   LayerTable t;
   st = make_table(p, layer, N, p->mode == FIB_MODE_INTERP ? alpha_dev : nullptr, &t);
   if (st != FIB_OK) return st;
+  corrupt_for_test(p, &t);
   return cuda_status(launch_fwd_tc(t, B, H, N, q, workspace, o, lse, p->d_lo, p->d_hi, p->d_status,
                                    p->wait_ns, p->skip_first_rung_copy, false,
                                    static_cast<cudaStream_t>(stream)));
+}
+
+size_t fib_attn_dense_fwd_workspace_size(fib_attn_plan_t p, int B, int H, int N, int dtype) {
+  if (p == nullptr || B < 1 || H < 1 || N < 1 || dtype != FIB_DTYPE_BF16) return 0;
+  return fwd_tc_workspace_bytes(B, H, N);
+}
+
+int fib_attn_dense_fwd(fib_attn_plan_t p, int B, int H, int N, int dtype, const void* q, const void* k,
+                       const void* v, void* o, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  int st = check_shape(p, 0, B, H, N, dtype);
+  if (st != FIB_OK) return st;
+  if (dtype != FIB_DTYPE_BF16) return FIB_ERR_UNSUPPORTED;
+  const size_t need = fib_attn_dense_fwd_workspace_size(p, B, H, N, dtype);
+  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < need) return FIB_ERR_INVALID_ARG;
+  if (workspace == q || workspace == k || workspace == v || workspace == o) return FIB_ERR_INVALID_ARG;
+  if (check_tensor(q) || check_tensor(k) || check_tensor(v) || check_tensor(o)) return FIB_ERR_INVALID_ARG;
+  if (o == q || o == k || o == v) return FIB_ERR_INVALID_ARG;
+  if (lse != nullptr && !aligned(lse, 4)) return FIB_ERR_INVALID_ARG;
+  st = check_device(p);
+  if (st != FIB_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = launch_prep_kv(B, H, N, k, v, p->d_lo, p->d_hi, workspace, p->d_status, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_dense_fwd(B, H, N, q, workspace, o, lse, p->d_lo, p->d_hi, p->d_status, p->wait_ns,
+                                      true, s));
 }
 
 int fib_attn_decode(fib_attn_plan_t p, int layer, int B, int H, int N, int pos, int dtype,
@@ -482,9 +525,11 @@ int fib_attn_debug_indices(fib_attn_plan_t p, int layer, int N, int i_begin, int
                                           static_cast<cudaStream_t>(stream)));
 }
 
-int fib_attn_plan_set_debug(fib_attn_plan_t p, int skip_first_rung_copy, long long wait_ns) {
+int fib_attn_plan_set_debug(fib_attn_plan_t p, int debug_flags, long long wait_ns) {
   if (p == nullptr || wait_ns < 1000 || wait_ns > 60LL * 1000000000LL) return FIB_ERR_INVALID_ARG;
-  p->skip_first_rung_copy = skip_first_rung_copy ? 1 : 0;
+  if (debug_flags & ~(FIB_DEBUG_SKIP_COPY | FIB_DEBUG_CORRUPT_TABLE)) return FIB_ERR_INVALID_ARG;
+  p->skip_first_rung_copy = (debug_flags & FIB_DEBUG_SKIP_COPY) ? 1 : 0;
+  p->corrupt_rung_table = (debug_flags & FIB_DEBUG_CORRUPT_TABLE) ? 1 : 0;
   p->wait_ns = static_cast<unsigned long long>(wait_ns);
   return FIB_OK;
 }

@@ -14,8 +14,6 @@
 //   dalpha = fixed-order sum of the CTA partials          (dalpha_reduce_kernel)
 // Both main kernels recompute scores from raw Q/K with the relative RoPE factors
 // (see fwd.cu), so no attention matrix is stored.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace fibattn {
@@ -334,29 +332,17 @@ cudaError_t launch_bwd(const LayerTable& t, int B, int H, int N, int dtype, cons
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchBytes];
 
-namespace {
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kNoAllocMaxDevices] = {};
-}  // namespace
-
 // Device address of the scratch array on the current device.  In host code the array's
-// name is only a host-side stand-in, never a device address, so the first call on a device
-// looks the address up with cudaGetSymbolAddress (with that device current) and caches it;
-// later calls on that device reuse the cached pointer.
+// name is only a host-side stand-in, never a device address, so every call looks the
+// address up with cudaGetSymbolAddress (with the caller's device current) and checks the
+// result.  Nothing is cached, so a context torn down and created again (cudaDeviceReset)
+// never leaves a stale address behind.
 cudaError_t noalloc_scratch(void** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_bwd_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_bwd_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  if (p == nullptr) return cudaErrorInvalidSymbol;
+  *out = p;
   return cudaSuccess;
 }
 

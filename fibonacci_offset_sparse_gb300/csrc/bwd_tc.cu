@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
                                                        __half* __restrict__ dos, float* __restrict__ delta,
                                                        const float2* __restrict__ lo_tab,
                                                        const float2* __restrict__ hi_tab, int N, long long rows,
-                                                       float qscale) {
+                                                       float qscale, int* __restrict__ status) {
   // The dependent dQ grid may launch at once (its CTAs take the SMs as this grid drains);
   // it waits for the whole of this grid before it reads what this grid writes.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -163,13 +163,22 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
     r4[u ^ sw] = lo4;
     r4[(u + 4) ^ sw] = hi4;
   };
+  // A value beyond the float16 range (|x| > 65504 after rotation and scaling) cannot be held
+  // in the prepared rows: record it (the gradients of this call are then unspecified).
+  uint32_t bad = 0;
+  auto chk = [&](const uint4& x) { bad |= h2_nonfinite(x.x) | h2_nonfinite(x.y) | h2_nonfinite(x.z) | h2_nonfinite(x.w); };
   uint4 ya, yb;
   rotate(qa, qb, qscale, ya, yb);
+  chk(ya); chk(yb);
   put(qs, ya, yb);
   rotate(ka, kb, 1.f, ya, yb);
+  chk(ya); chk(yb);
   put(kp, ya, yb);
-  put(vp, to_h(va), to_h(vb));
-  put(dos, to_h(ga), to_h(gb));
+  const uint4 vha = to_h(va), vhb = to_h(vb), gha = to_h(ga), ghb = to_h(gb);
+  chk(vha); chk(vhb); chk(gha); chk(ghb);
+  put(vp, vha, vhb);
+  put(dos, gha, ghb);
+  if (bad) atomicExch(status, kStatusRange);
   // Delta = dO . O over the row (float32 from the bf16 values)
   float d = 0.f;
   const uint32_t g4[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
 #pragma unroll
     for (int s = 0; s < kBSlots; ++s)
       if (last_n[s] >= 0) mbar_wait(&full_bar[s], (last_n[s] / kBSlots) & 1, a.wait_ns);
-    if (s_err) atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
+    if (s_err) atomicExch(a.status, kStatusTimeout);
     return;
   }
 
@@ -286,7 +295,7 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
   auto wait_stage = [&](int n) {
     if (!s_err && !mbar_wait(&full_bar[n % kBSlots], (n / kBSlots) & 1, a.wait_ns)) {
       s_err = 1;
-      atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
+      atomicExch(a.status, kStatusTimeout);
     }
   };
   auto release_stage = [&](int n) {
@@ -589,7 +598,7 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
 #pragma unroll
     for (int s = 0; s < kBSlots; ++s)
       if (last_n[s] >= 0) mbar_wait(&full_bar[s], (last_n[s] / kBSlots) & 1, a.wait_ns);
-    if (s_err) atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
+    if (s_err) atomicExch(a.status, kStatusTimeout);
     return;
   }
 
@@ -600,7 +609,7 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
   auto wait_stage = [&](int n) {
     if (!s_err && !mbar_wait(&full_bar[n % kBSlots], (n / kBSlots) & 1, a.wait_ns)) {
       s_err = 1;
-      atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
+      atomicExch(a.status, kStatusTimeout);
     }
   };
   auto release_stage = [&](int n) {
@@ -790,7 +799,7 @@ cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* 
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), const_cast<__half*>(a.qs),
       const_cast<__half*>(a.kp), const_cast<__half*>(a.vp), const_cast<__half*>(a.dos), delta, lo_tab, hi_tab, N, rows,
-      kLog2e / 8.0f);
+      kLog2e / 8.0f, status);
   cudaError_t e;
   // query-owned: dq and the dalpha partials
   a.slab_rows = t.mode == 1 ? kBTileT + 8 : kBTileT;

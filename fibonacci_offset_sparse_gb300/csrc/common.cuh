@@ -217,6 +217,16 @@ __device__ __forceinline__ float quad_sum(float x) {
   return x;
 }
 
+// Codes a kernel records in the plan's status word (the fib_status values of the C ABI).
+constexpr int kStatusTimeout = 5;       // a bounded wait gave up
+constexpr int kStatusDeviceAssert = 6;  // a device-side check of the rung table failed
+constexpr int kStatusRange = 7;         // a value does not fit the float16 operands
+
+// Nonzero when either float16 half of w is infinite or NaN (exponent bits all ones).
+__device__ __forceinline__ uint32_t h2_nonfinite(uint32_t w) {
+  return static_cast<uint32_t>((~w & 0x7c00u) == 0u) | static_cast<uint32_t>((~w & 0x7c000000u) == 0u);
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

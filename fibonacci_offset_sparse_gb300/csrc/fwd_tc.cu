@@ -88,58 +88,105 @@ struct TcArgs {
   const float2* rope_lo;
   const float2* rope_hi;
   float qscale;                // log2(e)/sqrt(D)
-  int* status;                 // plan status word (FIB_ERR_TIMEOUT on a wait that gave up)
+  int* status;                 // plan status word: timeout, rung-table check, float16 range
   unsigned long long wait_ns;  // bound of every mbarrier wait
   int skip_first_rung_copy;    // test hook: never arrive on rung 0's stage
 };
 
 // ------------------------------------------------------------------ K', V' preparation
-// One thread per (row, quarter u): frequencies m = 8u .. 8u+7, i.e. chunks u (dims 8u..) and
-// u+4 (their rotate-half partners 32+8u..) of the K row, and the same two chunks of V.
-__global__ void __launch_bounds__(256) prep_kv_kernel(const __nv_bfloat16* __restrict__ k,
-                                                      const __nv_bfloat16* __restrict__ v,
-                                                      __half* __restrict__ kp, __half* __restrict__ vp,
-                                                      const float2* __restrict__ lo_tab,
-                                                      const float2* __restrict__ hi_tab, int N,
-                                                      long long rows) {
+// A warp prepares 32 consecutive rows: lane (j8 = lane/4, u = lane%4) handles rows
+// base + 8i + j8 (i < kPrepIters) and the frequencies m = 8u .. 8u+7, i.e. chunks u (dims
+// 8u..) and u+4 (their rotate-half partners 32+8u..) of the K row, and the same two chunks
+// of V.  Every load of the warp is issued first.  The RoPE factors e^{i p theta_m} of the
+// first row come from the factored tables; each later row of the lane sits 8 positions
+// further, so its factors are the previous ones times e^{i 8 theta_m} (one complex product
+// each, relative error ~1e-7 a step, far below the float16 rounding of K'), unless a new
+// sequence began in between (position < 8), where the tables are read again.  This keeps
+// the table reads at a few bytes a row instead of 128.
+constexpr int kPrepIters = 4;
+constexpr int kPrepThreads = 128;
+constexpr int kPrepRowsPerBlock = kPrepThreads / 4 * kPrepIters;  // 128
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kv_kernel(const __nv_bfloat16* __restrict__ k,
+                                                               const __nv_bfloat16* __restrict__ v,
+                                                               __half* __restrict__ kp, __half* __restrict__ vp,
+                                                               const float2* __restrict__ lo_tab,
+                                                               const float2* __restrict__ hi_tab, int N,
+                                                               long long rows, int* __restrict__ status) {
   // The dependent attention grid may launch at once: its CTAs take the SMs as this grid
   // drains and load and rotate their Q rows meanwhile; each waits for the whole of this grid
   // (griddepcontrol.wait) before it reads K'/V'.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  const long long gid = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
-  const long long row = gid >> 2;
-  if (row >= rows) return;
-  const int u = static_cast<int>(gid & 3);
-  const int p = static_cast<int>(row % N);
-  const uint4* k4 = reinterpret_cast<const uint4*>(k + row * kD);
-  const uint4* v4 = reinterpret_cast<const uint4*>(v + row * kD);
-  const uint4 ka = __ldcs(k4 + u), kb = __ldcs(k4 + u + 4), va = __ldcs(v4 + u), vb = __ldcs(v4 + u + 4);
+  const int lane = threadIdx.x & 31;
+  const int u = lane & 3, j8 = lane >> 2;
+  const long long base = static_cast<long long>(blockIdx.x) * kPrepRowsPerBlock + (threadIdx.x >> 5) * 32 + j8;
+  uint4 ka[kPrepIters], kb[kPrepIters], va[kPrepIters], vb[kPrepIters];
+#pragma unroll
+  for (int i = 0; i < kPrepIters; ++i) {
+    const long long row = base + 8 * i;
+    if (row < rows) {
+      const uint4* k4 = reinterpret_cast<const uint4*>(k + row * kD);
+      const uint4* v4 = reinterpret_cast<const uint4*>(v + row * kD);
+      ka[i] = __ldcs(k4 + u);
+      kb[i] = __ldcs(k4 + u + 4);
+      va[i] = __ldcs(v4 + u);
+      vb[i] = __ldcs(v4 + u + 4);
+    }
+  }
+  float2 step[8];  // e^{i 8 theta_m}: row 8 of the low table
+  {
+    const float4* s4 = reinterpret_cast<const float4*>(lo_tab + 8 * kFreq + 8 * u);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float4 x = __ldg(s4 + w);
+      step[2 * w] = make_float2(x.x, x.y);
+      step[2 * w + 1] = make_float2(x.z, x.w);
+    }
+  }
   float2 e[8];
-  rope_row(lo_tab, hi_tab, p, u, e);
-  const uint32_t xa[4] = {ka.x, ka.y, ka.z, ka.w}, xb[4] = {kb.x, kb.y, kb.z, kb.w};
-  uint32_t ya[4], yb[4];
+  uint32_t bad = 0;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    // (k_m, k_{m+32}) -> (k_m cos - k_{m+32} sin, k_m sin + k_{m+32} cos), m = 8u + 2c (+1)
-    const float k1x = bf_lo(xa[c]), k1y = bf_hi(xa[c]), k2x = bf_lo(xb[c]), k2y = bf_hi(xb[c]);
-    const float2 e0 = e[2 * c], e1 = e[2 * c + 1];
-    ya[c] = pack_h2(k1x * e0.x - k2x * e0.y, k1y * e1.x - k2y * e1.y);
-    yb[c] = pack_h2(k1x * e0.y + k2x * e0.x, k1y * e1.y + k2y * e1.x);
-  }
-  const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
-  uint32_t za[4], zb[4];
+  for (int i = 0; i < kPrepIters; ++i) {
+    const long long row = base + 8 * i;
+    if (row >= rows) break;
+    const int p = static_cast<int>(row % N);
+    if (i == 0 || p < 8) {
+      rope_row(lo_tab, hi_tab, p, u, e);
+    } else {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    za[c] = pack_h2(bf_lo(wa[c]), bf_hi(wa[c]));
-    zb[c] = pack_h2(bf_lo(wb[c]), bf_hi(wb[c]));
+      for (int w = 0; w < 8; ++w)
+        e[w] = make_float2(e[w].x * step[w].x - e[w].y * step[w].y, e[w].x * step[w].y + e[w].y * step[w].x);
+    }
+    const uint32_t xa[4] = {ka[i].x, ka[i].y, ka[i].z, ka[i].w}, xb[4] = {kb[i].x, kb[i].y, kb[i].z, kb[i].w};
+    uint32_t ya[4], yb[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      // (k_m, k_{m+32}) -> (k_m cos - k_{m+32} sin, k_m sin + k_{m+32} cos), m = 8u + 2c (+1)
+      const float k1x = bf_lo(xa[c]), k1y = bf_hi(xa[c]), k2x = bf_lo(xb[c]), k2y = bf_hi(xb[c]);
+      const float2 e0 = e[2 * c], e1 = e[2 * c + 1];
+      ya[c] = pack_h2(k1x * e0.x - k2x * e0.y, k1y * e1.x - k2y * e1.y);
+      yb[c] = pack_h2(k1x * e0.y + k2x * e0.x, k1y * e1.y + k2y * e1.x);
+    }
+    const uint32_t wa[4] = {va[i].x, va[i].y, va[i].z, va[i].w}, wb[4] = {vb[i].x, vb[i].y, vb[i].z, vb[i].w};
+    uint32_t za[4], zb[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      za[c] = pack_h2(bf_lo(wa[c]), bf_hi(wa[c]));
+      zb[c] = pack_h2(bf_lo(wb[c]), bf_hi(wb[c]));
+    }
+    // A rotated key or a value beyond the float16 range (|x| > 65504) cannot be represented
+    // in the prepared rows: record it (the outputs of this call are then unspecified).
+#pragma unroll
+    for (int c = 0; c < 4; ++c) bad |= h2_nonfinite(ya[c]) | h2_nonfinite(yb[c]) | h2_nonfinite(za[c]) | h2_nonfinite(zb[c]);
+    const int sw = swz(p);
+    uint4* ko = reinterpret_cast<uint4*>(kp + row * kD);
+    uint4* vo = reinterpret_cast<uint4*>(vp + row * kD);
+    ko[u ^ sw] = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+    ko[(u + 4) ^ sw] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+    vo[u ^ sw] = make_uint4(za[0], za[1], za[2], za[3]);
+    vo[(u + 4) ^ sw] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
   }
-  const int sw = swz(p);
-  uint4* ko = reinterpret_cast<uint4*>(kp + row * kD);
-  uint4* vo = reinterpret_cast<uint4*>(vp + row * kD);
-  ko[u ^ sw] = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-  ko[(u + 4) ^ sw] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
-  vo[u ^ sw] = make_uint4(za[0], za[1], za[2], za[3]);
-  vo[(u + 4) ^ sw] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
+  if (bad) atomicExch(status, kStatusRange);
 }
 
 // ------------------------------------------------------------------ attention kernel
@@ -195,6 +242,28 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   auto rung_need = [&](int r) { return host_keys ? rung_lo(r) + (rung_w(r) > 0.f ? 1 : 0) : ks.need[W + r]; };
 
   const int warp = tid >> 5, lane = tid & 31;
+  // Device-side check of the rung table before any rung row is copied: every kept rung
+  // must lie beyond the window and inside the sequence (mask: W <= d <= N-1, strictly
+  // ascending; interp: W-1 < d = lo + w <= N-1, lo non-decreasing).  A table that breaks
+  // this records FIB_ERR_DEVICE_ASSERT and the CTA returns without writing output (the
+  // producer first lets its Q copy land).
+  {
+    bool bad = false;
+    if (lane < nr) {
+      const int lo = rung_lo(lane);
+      const float w = rung_w(lane);
+      const int prev = lane > 0 ? rung_lo(lane - 1) : -1;
+      if (MODE == 0) bad = lo < W || lo > N - 1 || lo <= prev;
+      else bad = lo < W - 1 || !(w >= 0.f && w < 1.f) || (lo == W - 1 && w == 0.f) || rung_need(lane) > N - 1 || lo < prev;
+    }
+    if (__any_sync(0xffffffffu, bad)) {  // the same vote in every warp
+      if (tid == kConsumers) {
+        mbar_wait(&full_bar[0], 0, a.wait_ns);
+        atomicExch(a.status, kStatusDeviceAssert);
+      }
+      return;
+    }
+  }
   // Rungs are kept in ascending distance; the tile streams rungs [0, nrt), up to the last one
   // that some row of it attends (a later tile attends more).
   const unsigned attended = __ballot_sync(0xffffffffu, lane < nr && rung_need(lane) <= i_last);
@@ -251,7 +320,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
 #pragma unroll
     for (int s = 0; s < kSlots; ++s)
       if (last_n[s] >= 0) mbar_wait(&full_bar[s], (last_n[s] / kSlots) & 1, a.wait_ns);
-    if (s_err) atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
+    if (s_err) atomicExch(a.status, kStatusTimeout);
     return;
   }
 
@@ -269,7 +338,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   auto wait_stage = [&](int n) {
     if (!s_err && !mbar_wait(&full_bar[n % kSlots], (n / kSlots) & 1, a.wait_ns)) {
       s_err = 1;
-      atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
+      atomicExch(a.status, kStatusTimeout);
     }
   };
   auto release_stage = [&](int n) {
@@ -311,6 +380,12 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
       qa[h][0][s] = pack_h2(y[2 * s], y[2 * s + 1]);
       qa[h][1][s] = pack_h2(y[8 + 2 * s], y[8 + 2 * s + 1]);
     }
+  }
+  {
+    uint32_t bad = 0;  // a scaled, rotated query beyond the float16 range
+#pragma unroll
+    for (int s = 0; s < 4; ++s) bad |= h2_nonfinite(qa[0][0][s]) | h2_nonfinite(qa[0][1][s]) | h2_nonfinite(qa[1][0][s]) | h2_nonfinite(qa[1][1][s]);
+    if (bad) atomicExch(a.status, kStatusRange);
   }
   release_stage(0);
 
@@ -539,7 +614,7 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   for (int r = n_near; r < nrt; ++r) {
     if (!s_err && !mbar_wait(&full_bar[slot], par, a.wait_ns)) {
       s_err = 1;
-      atomicExch(a.status, 5 /* FIB_ERR_TIMEOUT */);
+      atomicExch(a.status, kStatusTimeout);
     }
     const unsigned char* st = ring + slot * a.slot_bytes;
     float sc[2] = {-INFINITY, -INFINITY};
@@ -609,15 +684,15 @@ size_t fwd_tc_workspace_bytes(int B, int H, int N) {
 }
 
 cudaError_t launch_prep_kv(int B, int H, int N, const void* k, const void* v, const float2* lo_tab,
-                           const float2* hi_tab, void* workspace, cudaStream_t stream) {
+                           const float2* hi_tab, void* workspace, int* status, cudaStream_t stream) {
   const long long rows = static_cast<long long>(B) * H * N;
   __half* kp = static_cast<__half*>(workspace);
   __half* vp = kp + rows * kD;
-  const long long blocks = (rows * 4 + 255) / 256;  // four threads a row
+  const long long blocks = (rows + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  prep_kv_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+  prep_kv_kernel<<<static_cast<unsigned>(blocks), kPrepThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), kp, vp, lo_tab, hi_tab, N,
-      rows);
+      rows, status);
   return cudaGetLastError();
 }
 

@@ -16,7 +16,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfibattn.so")
 
 FIB_OK, FIB_ERR_INVALID_ARG, FIB_ERR_UNSUPPORTED, FIB_ERR_CUDA, FIB_ERR_NOMEM, \
-    FIB_ERR_TIMEOUT, FIB_ERR_DEVICE_ASSERT = range(7)
+    FIB_ERR_TIMEOUT, FIB_ERR_DEVICE_ASSERT, FIB_ERR_RANGE = range(8)
+FIB_DEBUG_SKIP_COPY, FIB_DEBUG_CORRUPT_TABLE = 1, 2
 FIB_BASE_FIBONACCI, FIB_BASE_POW2, FIB_BASE_CUSTOM = 0, 1, 2
 FIB_SCHED_FIXED, FIB_SCHED_LINEAR, FIB_SCHED_COPRIME = 0, 1, 2
 FIB_MODE_MASK, FIB_MODE_INTERP = 0, 1
@@ -29,7 +30,7 @@ EXPORTS = [
     "fib_attn_plan_distances", "fib_attn_fwd_workspace_size", "fib_attn_fwd",
     "fib_attn_fwd_prepare_kv", "fib_attn_fwd_attend", "fib_attn_bwd_workspace_size", "fib_attn_bwd",
     "fib_attn_debug_indices", "fib_attn_last_device_status", "fib_attn_plan_set_debug",
-    "fib_attn_bwd_noalloc", "fib_attn_decode",
+    "fib_attn_bwd_noalloc", "fib_attn_decode", "fib_attn_dense_fwd_workspace_size", "fib_attn_dense_fwd",
 ]
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -61,6 +62,8 @@ _SIGS = {
     "fib_attn_last_device_status": (_i, [_vp]),
     "fib_attn_plan_set_debug": (_i, [_vp, _i, ctypes.c_longlong]),
     "fib_attn_decode": (_i, [_vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "fib_attn_dense_fwd_workspace_size": (ctypes.c_size_t, [_vp, _i, _i, _i, _i]),
+    "fib_attn_dense_fwd": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "fib_attn_bwd_noalloc": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                   _vp, _vp, _vp, _vp]),
 }
@@ -259,6 +262,24 @@ def fib_attn_fwd_attend(plan: Plan, layer: int, q, workspace, o=None, lse=None, 
     return o, lse
 
 
+def fib_attn_dense_fwd(plan: Plan, q, k, v, o=None, lse=None, want_lse: bool = True, workspace=None,
+                       stream=None):
+    """Dense causal attention with the plan's RoPE (bf16); returns (o, lse)."""
+    B, H, N = _shape(q)
+    _same(q, k, v, o)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    need = int(lib().fib_attn_dense_fwd_workspace_size(plan.handle, B, H, N, _DT[q.dtype]))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check("fib_attn_dense_fwd", lib().fib_attn_dense_fwd(
+        plan.handle, B, H, N, _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return o, lse
+
+
 def fib_attn_decode(plan: Plan, layer: int, pos: int, q, k_cache, v_cache, o=None, lse=None,
                     alpha_dev=None, want_lse: bool = True, stream=None):
     """One token at position pos: q [B, H, 64], caches [B, H, N, 64]; returns (o, lse)."""
@@ -323,9 +344,11 @@ def fib_attn_debug_indices(plan: Plan, layer: int, N: int, i_begin: int, i_end: 
     return out, w
 
 
-def fib_attn_plan_set_debug(plan: Plan, skip_first_rung_copy: bool, wait_ns: int):
-    _check("fib_attn_plan_set_debug", lib().fib_attn_plan_set_debug(
-        plan.handle, 1 if skip_first_rung_copy else 0, int(wait_ns)))
+def fib_attn_plan_set_debug(plan: Plan, skip_first_rung_copy: bool, wait_ns: int,
+                            corrupt_table: bool = False):
+    flags = (FIB_DEBUG_SKIP_COPY if skip_first_rung_copy else 0) | \
+        (FIB_DEBUG_CORRUPT_TABLE if corrupt_table else 0)
+    _check("fib_attn_plan_set_debug", lib().fib_attn_plan_set_debug(plan.handle, flags, int(wait_ns)))
 
 
 def fib_attn_last_device_status(plan: Plan) -> int:

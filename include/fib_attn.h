@@ -55,8 +55,13 @@ enum fib_status {
   FIB_ERR_CUDA = 3,          /* a CUDA runtime call failed (incl. no device)            */
   FIB_ERR_NOMEM = 4,         /* host or device allocation failed                        */
   FIB_ERR_TIMEOUT = 5,       /* a bounded device wait gave up (see last_device_status)  */
-  FIB_ERR_DEVICE_ASSERT = 6  /* a device-side check recorded a violated invariant       */
+  FIB_ERR_DEVICE_ASSERT = 6, /* a device-side check recorded a violated invariant       */
+  FIB_ERR_RANGE = 7          /* an input value does not fit the float16 operands of the
+                                bf16 tensor-core path (see fib_attn_fwd)                */
 };
+
+/* Test hooks of fib_attn_plan_set_debug (bit flags). */
+enum fib_debug_flag { FIB_DEBUG_SKIP_COPY = 1, FIB_DEBUG_CORRUPT_TABLE = 2 };
 
 enum fib_base_kind { FIB_BASE_FIBONACCI = 0, FIB_BASE_POW2 = 1, FIB_BASE_CUSTOM = 2 };
 enum fib_schedule_kind { FIB_SCHED_FIXED = 0, FIB_SCHED_LINEAR = 1, FIB_SCHED_COPRIME = 2 };
@@ -68,7 +73,8 @@ enum fib_dtype { FIB_DTYPE_F32 = 0, FIB_DTYPE_BF16 = 1 };
 #define FIB_MAX_WINDOW 64 /* largest window W */
 #define FIB_MAX_LAYERS 256
 
-/* Human-readable name of a status code (static storage; never NULL). */
+/* Human-readable name of a status code (static storage; never NULL).  No counterpart in
+ * the paper. */
 const char* fib_attn_error_string(int code);
 
 /* ---------------------------------------------------------------- host-only planner --
@@ -102,6 +108,10 @@ int fib_attn_interp_rungs(const int32_t* base, int n_base, double alpha, int W, 
                           int* n_out);
 
 /* ------------------------------------------------------------------------- plan ----
+ * Defines the attended set of every layer of a stack: "Attended set" (a dense local window
+ * of W keys plus the Fibonacci offsets), "Scaling" (d_k = alpha_l f_k with one alpha per
+ * layer), "Experimental variables" (the per-layer alpha of a schedule, or a learned one),
+ * "Controls" (the power-of-two base) and "Implementation" (RoPE before the gather).
  * A plan fixes (base, per-layer alpha, W, N_max, D, mode, RoPE base) for a layer stack
  * and uploads the RoPE tables (built in binary64 on the host, stored float32) for
  * positions < N_max to the current device.  base_kind CUSTOM reads custom_base[n_custom]
@@ -113,15 +123,21 @@ int fib_attn_plan_create(fib_attn_plan_t* out, int base_kind, const int32_t* cus
                          int n_custom, const double* alpha, int n_layers, int W, int N_max,
                          int D, int mode, double rope_base);
 
-/* Frees the plan and its device tables (synchronises the device first).  NULL is OK. */
+/* Frees the plan and its device tables (synchronises the device first).  NULL is OK.
+ * No counterpart in the paper.                                                        */
 int fib_attn_plan_destroy(fib_attn_plan_t p);
 
 /* Host copy of the MASK distances (mode MASK) or INTERP lo values (mode INTERP) that the
- * plan uses for `layer` at sequence length N (N <= N_max).                             */
+ * plan uses for `layer` at sequence length N (N <= N_max): "Scaling" (d_k = alpha_l f_k)
+ * after the readings above.                                                            */
 int fib_attn_plan_distances(fib_attn_plan_t p, int layer, int N, int32_t* out, int cap,
                             int* n_out);
 
 /* ---------------------------------------------------------------------- forward ----
+ * The layer's sparse attention: "Attended set" and "Scaling" give the keys each query
+ * attends, "Implementation" the RoPE before the gather and the interpolated rows of a
+ * non-integer distance, Key results 2 > "Efficiency" the two paths (MASK: integer distances
+ * as a fused boolean mask; INTERP: the interpolated gather).
  * O = attention output (dtype of the inputs), lse = natural-log sum of exp(scores),
  * both for layer `layer` of the plan at sequence length N (1 <= N <= N_max).
  * q, k, v, o: [B, H, N, 64] device, dtype `dtype`.  lse: [B, H, N] float32 device, or
@@ -141,11 +157,21 @@ int fib_attn_fwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
                  const void* q, const void* k, const void* v, void* o, float* lse,
                  const float* alpha_dev, void* workspace, size_t ws_bytes, void* stream);
 
-/* The two halves of the bf16 forward, for callers that reuse the prepared keys and values
+/* Float16 range of the bf16 tensor-core path (bf16 with W <= 16; forward and backward):
+ * its operands are float16, so every value it converts must satisfy |x| <= 65504: the
+ * keys after RoPE, the values, the queries after RoPE times log2(e)/8 and, in the
+ * backward, dO and dS = P (dO . v~ - Delta).  A query, key, value or dO beyond that (or not
+ * finite) makes the call record FIB_ERR_RANGE in the plan's status word (read with
+ * fib_attn_last_device_status); the outputs of that call are then unspecified and may be
+ * infinite or NaN.  Values below 6.1e-5 in magnitude are held as float16 subnormals
+ * (absolute spacing 6e-8).  Float32 inputs and bf16 with W > 16 take the CUDA-core
+ * kernels, which compute in float32 and have no such limit.
+ *
+ * The two halves of the bf16 forward, for callers that reuse the prepared keys and values
  * (several query sets against one K/V) or time the halves apart.  fib_attn_fwd(...) ==
  * fib_attn_fwd_prepare_kv then fib_attn_fwd_attend on the same stream, bit for bit.
  * prepare_kv writes into workspace (sized by fib_attn_fwd_workspace_size) K rotated at each
- * row's own position (the RoPE of "Attended set": keys rotated before they are gathered)
+ * row's own position ("Implementation": RoPE is applied before the rows are gathered)
  * and V, both as float16 [B, H, N, 64]; its layout inside the workspace is private to the
  * library.  attend reads q and a workspace that prepare_kv filled for the same plan, B, H
  * and N (not checked) and writes o and lse as fib_attn_fwd.  Both return
@@ -156,6 +182,22 @@ int fib_attn_fwd_prepare_kv(fib_attn_plan_t p, int B, int H, int N, int dtype, c
 int fib_attn_fwd_attend(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
                         const void* q, const void* workspace, size_t ws_bytes, void* o,
                         float* lse, const float* alpha_dev, void* stream);
+
+/* ------------------------------------------------------------------ dense control ----
+ * Dense causal attention with the same RoPE and scale: every query i attends every key
+ * j <= i (Methodology > "Controls": a dense model of the same architecture as the upper
+ * bound; Key results 3: dense attention at 4x the training length).  It equals fib_attn_fwd
+ * of a plan whose window covers the sequence (W >= N), but runs the dense blocked kernel.
+ * The plan supplies only its RoPE tables (N <= N_max) and status word; its layers, window
+ * and rungs play no part.  bf16 only (FIB_ERR_UNSUPPORTED for float32); q, k, v, o, lse
+ * and the errors as fib_attn_fwd; workspace: at least
+ * fib_attn_dense_fwd_workspace_size(p, B, H, N, dtype) bytes (B*H*N*256 for bf16, the
+ * rotated keys and the values as float16), 256-byte aligned, caller-owned.  The float16
+ * range rule of the bf16 path applies.                                                  */
+size_t fib_attn_dense_fwd_workspace_size(fib_attn_plan_t p, int B, int H, int N, int dtype);
+int fib_attn_dense_fwd(fib_attn_plan_t p, int B, int H, int N, int dtype, const void* q,
+                       const void* k, const void* v, void* o, float* lse, void* workspace,
+                       size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ decode ----
  * One new token per (b, h) against a KV cache (Key results 2, "Efficiency": inference
@@ -171,6 +213,8 @@ int fib_attn_decode(fib_attn_plan_t p, int layer, int B, int H, int N, int pos, 
                     const float* alpha_dev, void* stream);
 
 /* --------------------------------------------------------------------- backward ----
+ * "Implementation": the interpolated rows make the output differentiable in alpha, and
+ * "Experimental variables" > learned: alpha is then a trained per-layer parameter.
  * Gradients of l = sum(O * dO) for one layer, given the forward's o and lse.
  * dq, dk, dv: [B, H, N, 64] device (dtype of the inputs), fully written.
  * dalpha: device float32 scalar, written (not accumulated) with dl/dalpha_layer in
@@ -197,38 +241,52 @@ int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
  * scratch is a fixed 8 MiB device array inside the library, held on every device that
  * loads it until the process exits.  A call whose CUDA-core scratch (4 bytes per
  * query-head plus 4 per 64-query tile) exceeds 8 MiB, i.e. B*H*N above about two million,
- * returns FIB_ERR_INVALID_ARG before any launch.  The first call on a device looks
- * up the array's device address and caches it (host-side work; make that first call before
- * any stream capture).  Every call shares the array and it keeps the last call's contents
- * (nothing in it needs zeroing); calls whose kernels overlap on the GPU race on it.  Nothing
- * is allocated, by the library or through CUDA.                                           */
+ * returns FIB_ERR_INVALID_ARG before any launch.  Every call looks up the array's device
+ * address on the current device (cudaGetSymbolAddress, host-side work); the first call on a
+ * device may also load the library's device code there, so make that first call before any
+ * stream capture.  The address is not cached, so a call after a device reset still finds
+ * the array.  Every call shares the array and it keeps the last call's contents (nothing
+ * in it needs zeroing); calls whose kernels overlap on the GPU race on it.  Nothing is
+ * allocated, by the library or through CUDA.                                              */
 int fib_attn_bwd_noalloc(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
                          const void* q, const void* k, const void* v, const void* o,
                          const float* lse, const void* dO, void* dq, void* dk, void* dv,
                          float* dalpha, const float* alpha_dev, void* stream);
 
 /* ---------------------------------------------------------------- debug / status ----
- * The attended index sets of queries [i_begin, i_end), produced by the same device
+ * The attended index sets ("Attended set"; INTERP: the two bracketing rows of
+ * "Implementation") of queries [i_begin, i_end), produced by the same device
  * index code as the forward kernel.  out_dev: int32 [(i_end-i_begin), W + FIB_MAX_RUNGS]
  * device; slot s < W holds the window row i-s, slot W+r holds rung r's row (MASK: i-d;
  * INTERP: i-lo, whose partner row i-lo-1 carries weight w), -1 where not attended.
- * w_out_dev: float32 [FIB_MAX_RUNGS] device (INTERP weights; 0 for MASK) or NULL.      */
+ * w_out_dev: float32 [FIB_MAX_RUNGS] device (INTERP weights; 0 for MASK) or NULL.
+ * alpha_dev as fib_attn_fwd (INTERP: the device float32 alpha the forward would use, or
+ * NULL for the plan's).  Errors: FIB_ERR_INVALID_ARG (layer, N, an empty or out-of-range
+ * query range, misaligned pointers), FIB_ERR_CUDA.                                      */
 int fib_attn_debug_indices(fib_attn_plan_t p, int layer, int N, int i_begin, int i_end,
                            int32_t* out_dev, float* w_out_dev, const float* alpha_dev,
                            void* stream);
 
-/* Wait bound and fault-injection hook of the plan's kernels.  Kernels that stage rows with
- * the bulk-copy engine wait on mbarriers; every such wait gives up after wait_ns
- * nanoseconds (default 1e9; accepted range [1e3, 6e10]), records FIB_ERR_TIMEOUT in the
- * status word, lets the copies already in flight land and returns without writing output.
- * skip_first_rung_copy != 0 makes the bf16 forward never complete one of its staged copies
- * (the values of the window block), so that a test can drive that timeout path without any
- * device fault.  Host-only; takes
- * effect on the next launch.  FIB_ERR_INVALID_ARG on a null plan or wait_ns out of range.   */
-int fib_attn_plan_set_debug(fib_attn_plan_t p, int skip_first_rung_copy, long long wait_ns);
+/* Wait bound and test hooks of the plan's kernels (no counterpart in the paper: they
+ * exist so that the error paths can be driven without any device fault).  Kernels that
+ * stage rows with the bulk-copy engine wait on mbarriers; every such wait gives up after
+ * wait_ns nanoseconds (default 1e9; accepted range [1e3, 6e10]), records FIB_ERR_TIMEOUT in
+ * the status word, lets the copies already in flight land and returns without writing
+ * output.  debug_flags: FIB_DEBUG_SKIP_COPY makes the bf16 tensor-core forward never
+ * complete one of its staged copies (the values of the window block), which drives that
+ * timeout path; FIB_DEBUG_CORRUPT_TABLE moves the first rung of the bf16 tensor-core
+ * forward's host-built rung table to distance 0 (a row inside the window, so every address
+ * stays inside the sequence), which its device-side table check rejects with
+ * FIB_ERR_DEVICE_ASSERT before any rung row is read.  Host-only; takes effect on the next
+ * launch.  FIB_ERR_INVALID_ARG on a null plan, an unknown flag or wait_ns out of range.   */
+int fib_attn_plan_set_debug(fib_attn_plan_t p, int debug_flags, long long wait_ns);
 
-/* Synchronises the plan's device, then returns and clears the device status word:
- * FIB_OK, FIB_ERR_TIMEOUT (a bounded wait gave up) or FIB_ERR_DEVICE_ASSERT.          */
+/* Synchronises the plan's device, then returns and clears the device status word (no
+ * counterpart in the paper): FIB_OK, FIB_ERR_TIMEOUT (a bounded wait gave up),
+ * FIB_ERR_DEVICE_ASSERT (the tensor-core forward's check of its rung table: every rung
+ * beyond the window and inside the sequence, in ascending order) or FIB_ERR_RANGE (a value
+ * outside the float16 range, see fib_attn_fwd).  Where several calls recorded a code, the
+ * last one written is returned.                                                        */
 int fib_attn_last_device_status(fib_attn_plan_t p);
 
 #ifdef __cplusplus

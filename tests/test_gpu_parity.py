@@ -93,14 +93,17 @@ def _rel_l2(a, b):
 
 
 def _run_fwd(kind, alphas, W, B, H, N, dtype, mode, layers, config, alpha_dev=None, heads=None):
+    """Forward of every listed layer at the full shape; the oracle on all heads, or on the
+    head slice `heads` (a slice, or a function of the layer giving one)."""
     plan = _plan(kind, alphas, W, N, mode)
     adev = None if alpha_dev is None else torch.tensor(alpha_dev, dtype=torch.float32, device="cuda")
     for layer in layers:
         q, k, v = inputs.qkv(B, H, N, 64, config, layer, dtype)
         o, lse = fa.fib_attn_fwd(plan, layer, q.cuda(), k.cuda(), v.cuda(), alpha_dev=adev)
         torch.cuda.synchronize()
+        assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
         a = alphas[layer] if alpha_dev is None else float(np.float32(alpha_dev[layer]))
-        hs = slice(None) if heads is None else heads
+        hs = slice(None) if heads is None else (heads(layer) if callable(heads) else heads)
         O_ref, lse_ref = oracle.attend(inputs.as_f64(q[:, hs]), inputs.as_f64(k[:, hs]),
                                        inputs.as_f64(v[:, hs]), a, _base_fn(kind)(N), W, mode)
         _check_o(o[:, hs], O_ref, dtype, f"layer {layer}")
@@ -123,9 +126,12 @@ def test_c1_linear_stack_bf16():
 
 @pytest.mark.parametrize("kind", ["fib", "pow2"])
 def test_c2_coprime_extrapolation_bf16(kind):
-    """16 layers, B=2, H=8, N=4096, bf16, W=12, coprime schedule; layers sampled."""
+    """16 layers, B=2, H=8, N=4096, bf16, W=12, coprime schedule: every layer's forward at
+    the full shape (each layer its own alpha and rung table, 8 to 11 rungs), O and LSE against
+    the oracle on two of the eight heads of both batch rows, a different pair per layer, so
+    that the 16 layers cover every head twice."""
     _run_fwd(kind, oracle.schedule("coprime", 16), 12, 2, 8, 4096, "bf16", "mask",
-             [0, 7, 9, 15], 2 if kind == "fib" else 12)
+             range(16), 2 if kind == "fib" else 12, heads=lambda l: slice(2 * (l % 4), 2 * (l % 4) + 2))
 
 
 @pytest.mark.parametrize("mode", ["mask", "interp"])
@@ -161,6 +167,39 @@ def test_c3_learned_fwd_bwd_bf16():
             assert e <= REL_L2, f"layer {layer} {name} rel-L2 {e:.3e}"
         e = abs(float(da.item()) - ra) / max(abs(ra), 1e-30)
         _record("bwd_rel_dalpha", f"c3 layer {layer}", e)
+        assert e <= REL_L2, f"layer {layer} dalpha {da.item()} vs {ra} rel {e:.3e}"
+    plan.close()
+
+
+def test_c3_every_layer_fwd_bwd_bf16():
+    """The learned-dilation training step of every one of the 16 layers (W=10, Fibonacci,
+    alpha ~ U[0.9, 1.1] on the device, interp forward + backward), at N=1024 with B=2, H=2 so
+    that the oracle's full backward (dalpha sums every head) stays cheap: O, LSE, dQ, dK, dV
+    and dalpha of each layer against the oracle."""
+    L, B, H, N, W = 16, 2, 2, 1024, 10
+    alpha = inputs.learned_alpha(L, 3)
+    plan = _plan("fib", [1.0] * L, W, N, "interp")
+    adev = torch.tensor(alpha, dtype=torch.float32, device="cuda")
+    for layer in range(L):
+        q, k, v = inputs.qkv(B, H, N, 64, 31, layer, "bf16")
+        dO = inputs.upstream_grad(B, H, N, 64, 31, layer, "bf16")
+        qc, kc, vc, dOc = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+        o, lse = fa.fib_attn_fwd(plan, layer, qc, kc, vc, alpha_dev=adev)
+        dq, dk, dv, da = fa.fib_attn_bwd(plan, layer, qc, kc, vc, o, lse, dOc, alpha_dev=adev)
+        torch.cuda.synchronize()
+        assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+        a = float(alpha[layer])
+        qf, kf, vf, gf = (inputs.as_f64(x) for x in (q, k, v, dO))
+        O_ref, lse_ref = oracle.attend(qf, kf, vf, a, oracle.fibonacci_base(), W, "interp")
+        _check_o(o, O_ref, "bf16", f"c3 sweep layer {layer}")
+        _check_lse(lse, lse_ref, "bf16", f"c3 sweep layer {layer}")
+        rq, rk, rv, ra = oracle.attend_bwd(qf, kf, vf, gf, a, oracle.fibonacci_base(), W, "interp")
+        for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+            e = _rel_l2(g.double().cpu().numpy(), r)
+            _record("bwd_rel_l2_" + name, f"c3 sweep layer {layer}", e)
+            assert e <= REL_L2, f"layer {layer} {name} rel-L2 {e:.3e}"
+        e = abs(float(da.item()) - ra) / max(abs(ra), 1e-30)
+        _record("bwd_rel_dalpha", f"c3 sweep layer {layer}", e)
         assert e <= REL_L2, f"layer {layer} dalpha {da.item()} vs {ra} rel {e:.3e}"
     plan.close()
 
@@ -299,6 +338,41 @@ def test_backward_bf16_tensor_core(mode, alpha, W, N, device_alpha):
         _record("bwd_rel_dalpha", what, e)
         assert e <= REL_L2, f"{what} dalpha {da.item()} vs {ra} rel {e:.3e}"
     dq2, dk2, dv2, da2 = fa.fib_attn_bwd(plan, 0, qc, kc, vc, o, lse, dOc, alpha_dev=adev)
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2) and torch.equal(da, da2)
+    plan.close()
+
+
+@pytest.mark.parametrize("mode,alpha,W,N", [("mask", 0.9, 17, 333), ("interp", 1.2345, 17, 517),
+                                             ("mask", 1.37, 24, 300), ("interp", 0.7771, 24, 401)])
+def test_backward_bf16_cuda_core(mode, alpha, W, N):
+    """bf16 with a window wider than 16 takes the CUDA-core forward and backward (float32
+    arithmetic on the bf16 values): gradients against the oracle's, ragged N, and a second run
+    with identical bits."""
+    B, H = 2, 2
+    plan = _plan("fib", [alpha], W, N, mode)
+    q, k, v = inputs.qkv(B, H, N, 64, 220, W, "bf16")
+    dO = inputs.upstream_grad(B, H, N, 64, 220, W, "bf16")
+    qc, kc, vc, dOc = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+    o, lse = fa.fib_attn_fwd(plan, 0, qc, kc, vc)
+    dq, dk, dv, da = fa.fib_attn_bwd(plan, 0, qc, kc, vc, o, lse, dOc)
+    torch.cuda.synchronize()
+    qf, kf, vf, gf = (inputs.as_f64(x) for x in (q, k, v, dO))
+    O_ref, _ = oracle.attend(qf, kf, vf, alpha, oracle.fibonacci_base(), W, mode)
+    _check_o(o, O_ref, "bf16", f"cuda-core {mode} W={W}")
+    rq, rk, rv, ra = oracle.attend_bwd(qf, kf, vf, gf, alpha, oracle.fibonacci_base(), W, mode)
+    what = f"cuda-core {mode} alpha={alpha} W={W} N={N}"
+    for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        e = _rel_l2(g.double().cpu().numpy(), r)
+        _record("bwd_rel_l2_" + name, what, e)
+        assert e <= REL_L2, f"{what} {name} rel-L2 {e:.3e}"
+    if mode == "mask":
+        assert float(da.item()) == 0.0
+    else:
+        e = abs(float(da.item()) - ra) / max(abs(ra), 1e-30)
+        _record("bwd_rel_dalpha", what, e)
+        assert e <= REL_L2, f"{what} dalpha {da.item()} vs {ra} rel {e:.3e}"
+    dq2, dk2, dv2, da2 = fa.fib_attn_bwd(plan, 0, qc, kc, vc, o, lse, dOc)
     torch.cuda.synchronize()
     assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2) and torch.equal(da, da2)
     plan.close()
@@ -460,4 +534,81 @@ def test_graph_replay_of_a_stack_with_varying_rung_counts():
     for l in range(16):
         assert torch.equal(outs[l], eager[l]), l
     assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    plan.close()
+
+
+# ------------------------------------------------------------------ device-side table check
+@pytest.mark.parametrize("mode", ["mask", "interp"])
+def test_corrupted_rung_table_is_rejected_on_the_device(mode):
+    """The test hook moves the first rung of the tensor-core forward's table to distance 0
+    (inside the window; every address it implies is still a row of the sequence).  The
+    kernel's table check records FIB_ERR_DEVICE_ASSERT and returns before any rung row is
+    read or any output written; the same context then runs a correct forward."""
+    B, H, N, W, alpha = 1, 2, 256, 12, 1.2345
+    plan = _plan("fib", [alpha], W, N, mode)
+    q, k, v = inputs.qkv(B, H, N, 64, 510, 0, "bf16")
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o = torch.full_like(qc, 7.0)
+    lse = torch.full((B, H, N), 7.0, device="cuda")
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    fa.fib_attn_plan_set_debug(plan, False, 1_000_000_000, corrupt_table=True)
+    fa.fib_attn_fwd(plan, 0, qc, kc, vc, o=o, lse=lse)
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_ERR_DEVICE_ASSERT
+    assert bool((o == 7.0).all()) and bool((lse == 7.0).all())  # nothing was written
+    fa.fib_attn_plan_set_debug(plan, False, 1_000_000_000)
+    o, lse = fa.fib_attn_fwd(plan, 0, qc, kc, vc)
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    O_ref, lse_ref = oracle.attend(inputs.as_f64(q), inputs.as_f64(k), inputs.as_f64(v), alpha,
+                                   oracle.fibonacci_base(), W, mode)
+    _check_o(o, O_ref, "bf16", "after table check")
+    _check_lse(lse, lse_ref, "bf16", "after table check")
+    assert fa.lib().fib_attn_plan_set_debug(plan.handle, 4, 1_000_000_000) == fa.FIB_ERR_INVALID_ARG  # unknown flag
+    plan.close()
+
+
+# ------------------------------------------------------------------ float16 range of the bf16 path
+def test_values_near_the_float16_limit_match_the_oracle():
+    """V scaled so that its largest magnitude is about 6e4 (inside float16's 65504): the
+    forward still matches the oracle on the same bf16 values.  O is linear in V, so the
+    absolute part of the bound scales with the factor; LSE does not depend on V."""
+    B, H, N, W, alpha = 2, 2, 333, 12, 1.2345
+    for mode in ("mask", "interp"):
+        plan = _plan("fib", [alpha], W, N, mode)
+        q, k, v = inputs.qkv(B, H, N, 64, 520, 0, "bf16")
+        s = 6.0e4 / float(v.float().abs().max())
+        v = (v.float() * s).to(torch.bfloat16)
+        assert float(v.float().abs().max()) <= 65504.0
+        o, lse = fa.fib_attn_fwd(plan, 0, q.cuda(), k.cuda(), v.cuda())
+        torch.cuda.synchronize()
+        assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+        O_ref, lse_ref = oracle.attend(inputs.as_f64(q), inputs.as_f64(k), inputs.as_f64(v), alpha,
+                                       oracle.fibonacci_base(), W, mode)
+        err = np.abs(o.double().cpu().numpy() - O_ref)
+        bound = BF16_ATOL * s + np.abs(O_ref) * 2.0 ** -8
+        assert np.all(err <= bound), (mode, float((err - bound).max()))
+        _check_lse(lse, lse_ref, "bf16", f"near float16 limit {mode}")
+        plan.close()
+
+
+@pytest.mark.parametrize("which", ["q", "k", "v"])
+def test_values_beyond_the_float16_limit_record_a_range_error(which):
+    """One element of q, k or v set to 1e6 (a bf16 value beyond float16's range once rotated
+    and scaled) makes the bf16 tensor-core forward and backward record FIB_ERR_RANGE; the
+    same context then runs a correct forward on in-range values."""
+    B, H, N, W, alpha = 1, 2, 200, 12, 1.0
+    plan = _plan("fib", [alpha], W, N, "mask")
+    q, k, v = inputs.qkv(B, H, N, 64, 530, 0, "bf16")
+    dO = inputs.upstream_grad(B, H, N, 64, 530, 0, "bf16")
+    big = {"q": q.clone(), "k": k.clone(), "v": v.clone()}
+    big[which][0, 1, 100, 5] = 1.0e6
+    xs = [big[n].cuda() for n in ("q", "k", "v")]
+    o, lse = fa.fib_attn_fwd(plan, 0, *xs)
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_ERR_RANGE
+    fa.fib_attn_bwd(plan, 0, *xs, o, lse, dO.cuda())
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_ERR_RANGE
+    o, lse = fa.fib_attn_fwd(plan, 0, q.cuda(), k.cuda(), v.cuda())
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    O_ref, _ = oracle.attend(inputs.as_f64(q), inputs.as_f64(k), inputs.as_f64(v), alpha,
+                             oracle.fibonacci_base(), W, "mask")
+    _check_o(o, O_ref, "bf16", "after range error")
     plan.close()

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(built_lib):
 
 
 def test_error_strings():
-    for code in range(7):
+    for code in range(8):
         assert fa.error_string(code)
     assert fa.error_string(99) == "unknown status"
 
