@@ -9,7 +9,13 @@ Tolerances:
     path rounds the RoPE-rotated Q' and K' to f16 (11-bit significand) for the window and
     every rung, so a 64-term score carries up to ~1e-3 of rounding error, which LSE
     inherits (the O bound above is the binding one);
-  * dQ, dK, dV, dalpha: relative L2 <= 2e-2.
+  * dQ, dK, dV: relative L2 <= 2e-2;
+  * dalpha (one scalar, a sum over batch rows and heads of contributions of both signs):
+    |error| <= 2e-2 times the larger of |dalpha| and the root-sum-square of its per-(b, h)
+    contributions, all from the oracle.  Where the heads' contributions cancel, |dalpha|
+    measures the cancellation rather than the kernel (in one seeded case four contributions
+    of 34e3, -19e3, -28e3 and 15e3 sum to 1.0e3, and rounding the forward's O to bf16 alone
+    moves that sum by 0.8 %), so the bound takes the scale of the contributions.
 """
 import json
 import math
@@ -92,6 +98,28 @@ def _rel_l2(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
+def _oracle_bwd(qf, kf, vf, gf, alpha, base, W, mode):
+    """The oracle's gradients, one (b, h) at a time (each head is independent): dq, dk, dv,
+    dalpha (the sum over heads) and the root-sum-square of the per-head dalpha contributions."""
+    B, H = qf.shape[:2]
+    rq, rk, rv = np.zeros_like(qf), np.zeros_like(kf), np.zeros_like(vf)
+    per = []
+    for b in range(B):
+        for h in range(H):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            gq, gk, gv, ga = oracle.attend_bwd(qf[sl], kf[sl], vf[sl], gf[sl], alpha, base, W, mode)
+            rq[sl], rk[sl], rv[sl] = gq, gk, gv
+            per.append(ga)
+    return rq, rk, rv, float(sum(per)), float(np.sqrt(np.sum(np.square(per))))
+
+
+def _check_dalpha(da, ra, rss, what):
+    err = abs(float(da.item()) - ra)
+    scale = max(abs(ra), rss)
+    _record("bwd_rel_dalpha", what, err / max(scale, 1e-30))
+    assert err <= REL_L2 * scale, f"{what} dalpha {da.item()} vs {ra} (per-head rss {rss:.4g})"
+
+
 def _run_fwd(kind, alphas, W, B, H, N, dtype, mode, layers, config, alpha_dev=None, heads=None):
     """Forward of every listed layer at the full shape; the oracle on all heads, or on the
     head slice `heads` (a slice, or a function of the layer giving one)."""
@@ -160,14 +188,12 @@ def test_c3_learned_fwd_bwd_bf16():
         _check_o(o, O_ref, "bf16", f"layer {layer}")
         _check_lse(lse, lse_ref, "bf16")
         # the backward consumes the kernel's bf16 O; the oracle differentiates its own forward
-        rq, rk, rv, ra = oracle.attend_bwd(qf, kf, vf, gf, a, oracle.fibonacci_base(), W, "interp")
+        rq, rk, rv, ra, rss = _oracle_bwd(qf, kf, vf, gf, a, oracle.fibonacci_base(), W, "interp")
         for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
             e = _rel_l2(g.double().cpu().numpy(), r)
             _record("bwd_rel_l2_" + name, f"c3 layer {layer}", e)
             assert e <= REL_L2, f"layer {layer} {name} rel-L2 {e:.3e}"
-        e = abs(float(da.item()) - ra) / max(abs(ra), 1e-30)
-        _record("bwd_rel_dalpha", f"c3 layer {layer}", e)
-        assert e <= REL_L2, f"layer {layer} dalpha {da.item()} vs {ra} rel {e:.3e}"
+        _check_dalpha(da, ra, rss, f"c3 layer {layer}")
     plan.close()
 
 
@@ -193,14 +219,12 @@ def test_c3_every_layer_fwd_bwd_bf16():
         O_ref, lse_ref = oracle.attend(qf, kf, vf, a, oracle.fibonacci_base(), W, "interp")
         _check_o(o, O_ref, "bf16", f"c3 sweep layer {layer}")
         _check_lse(lse, lse_ref, "bf16", f"c3 sweep layer {layer}")
-        rq, rk, rv, ra = oracle.attend_bwd(qf, kf, vf, gf, a, oracle.fibonacci_base(), W, "interp")
+        rq, rk, rv, ra, rss = _oracle_bwd(qf, kf, vf, gf, a, oracle.fibonacci_base(), W, "interp")
         for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
             e = _rel_l2(g.double().cpu().numpy(), r)
             _record("bwd_rel_l2_" + name, f"c3 sweep layer {layer}", e)
             assert e <= REL_L2, f"layer {layer} {name} rel-L2 {e:.3e}"
-        e = abs(float(da.item()) - ra) / max(abs(ra), 1e-30)
-        _record("bwd_rel_dalpha", f"c3 sweep layer {layer}", e)
-        assert e <= REL_L2, f"layer {layer} dalpha {da.item()} vs {ra} rel {e:.3e}"
+        _check_dalpha(da, ra, rss, f"c3 sweep layer {layer}")
     plan.close()
 
 
@@ -325,7 +349,7 @@ def test_backward_bf16_tensor_core(mode, alpha, W, N, device_alpha):
     torch.cuda.synchronize()
     assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
     qf, kf, vf, gf = (inputs.as_f64(x) for x in (q, k, v, dO))
-    rq, rk, rv, ra = oracle.attend_bwd(qf, kf, vf, gf, alpha, oracle.fibonacci_base(), W, mode)
+    rq, rk, rv, ra, rss = _oracle_bwd(qf, kf, vf, gf, alpha, oracle.fibonacci_base(), W, mode)
     what = f"{mode} alpha={alpha} W={W} N={N}"
     for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         e = _rel_l2(g.double().cpu().numpy(), r)
@@ -334,9 +358,7 @@ def test_backward_bf16_tensor_core(mode, alpha, W, N, device_alpha):
     if mode == "mask":
         assert float(da.item()) == 0.0
     else:
-        e = abs(float(da.item()) - ra) / max(abs(ra), 1e-30)
-        _record("bwd_rel_dalpha", what, e)
-        assert e <= REL_L2, f"{what} dalpha {da.item()} vs {ra} rel {e:.3e}"
+        _check_dalpha(da, ra, rss, what)
     dq2, dk2, dv2, da2 = fa.fib_attn_bwd(plan, 0, qc, kc, vc, o, lse, dOc, alpha_dev=adev)
     torch.cuda.synchronize()
     assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2) and torch.equal(da, da2)
@@ -360,7 +382,7 @@ def test_backward_bf16_cuda_core(mode, alpha, W, N):
     qf, kf, vf, gf = (inputs.as_f64(x) for x in (q, k, v, dO))
     O_ref, _ = oracle.attend(qf, kf, vf, alpha, oracle.fibonacci_base(), W, mode)
     _check_o(o, O_ref, "bf16", f"cuda-core {mode} W={W}")
-    rq, rk, rv, ra = oracle.attend_bwd(qf, kf, vf, gf, alpha, oracle.fibonacci_base(), W, mode)
+    rq, rk, rv, ra, rss = _oracle_bwd(qf, kf, vf, gf, alpha, oracle.fibonacci_base(), W, mode)
     what = f"cuda-core {mode} alpha={alpha} W={W} N={N}"
     for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         e = _rel_l2(g.double().cpu().numpy(), r)
@@ -369,9 +391,7 @@ def test_backward_bf16_cuda_core(mode, alpha, W, N):
     if mode == "mask":
         assert float(da.item()) == 0.0
     else:
-        e = abs(float(da.item()) - ra) / max(abs(ra), 1e-30)
-        _record("bwd_rel_dalpha", what, e)
-        assert e <= REL_L2, f"{what} dalpha {da.item()} vs {ra} rel {e:.3e}"
+        _check_dalpha(da, ra, rss, what)
     dq2, dk2, dv2, da2 = fa.fib_attn_bwd(plan, 0, qc, kc, vc, o, lse, dOc)
     torch.cuda.synchronize()
     assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2) and torch.equal(da, da2)
