@@ -52,6 +52,18 @@ size_t noalloc_scratch_bytes();
 
 using namespace fibattn;
 
+namespace {
+// Test hook: every CTA takes a whole SM's shared memory and fills it with `pattern`, so that
+// the kernels launched next on those SMs start from known stale contents.
+__global__ void fill_shared_kernel(uint32_t pattern, int words) {
+  extern __shared__ uint32_t fill_smem[];
+  for (int i = threadIdx.x; i < words; i += blockDim.x) fill_smem[i] = pattern;
+  __syncthreads();
+  // keep the stores: make them observable through a value no thread will ever see
+  if (fill_smem[(threadIdx.x * 7) % words] == pattern + 1u && pattern == 0xffffffffu) fill_smem[0] = 0u;
+}
+}  // namespace
+
 struct fib_attn_plan_s {
   int base_kind = 0;
   std::vector<int32_t> custom;
@@ -532,6 +544,19 @@ int fib_attn_plan_set_debug(fib_attn_plan_t p, int debug_flags, long long wait_n
   p->corrupt_rung_table = (debug_flags & FIB_DEBUG_CORRUPT_TABLE) ? 1 : 0;
   p->wait_ns = static_cast<unsigned long long>(wait_ns);
   return FIB_OK;
+}
+
+int fib_attn_debug_fill_shared(uint32_t pattern, void* stream) {
+  int dev = 0, sms = 0, smem = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(fill_shared_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_status(e);
+  // two waves of one CTA per SM, so that every SM is reached
+  fill_shared_kernel<<<2 * sms, 1024, static_cast<size_t>(smem), static_cast<cudaStream_t>(stream)>>>(
+      pattern, smem / 4);
+  return cuda_status(cudaGetLastError());
 }
 
 int fib_attn_last_device_status(fib_attn_plan_t p) {

@@ -348,8 +348,11 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
         const int c = 8 * nt + 2 * t + e;
         const int dist = g + 8 * h + 16 - c;
         const bool ok = dist >= 0 && dist < W && q0 - 16 + c >= 0;
+        // keys outside the copied window rows (before position 0, or after the tile's last
+        // row) were computed from stale shared memory: they are replaced, never multiplied,
+        // so that no stale NaN or infinity can reach dS through a product with p = 0
         const float p = ok ? exp2f(S[nt][2 * h + e] - lse2[h]) : 0.f;
-        S[nt][2 * h + e] = p * (D[nt][2 * h + e] - dlt[h]);  // dS
+        S[nt][2 * h + e] = ok ? p * (D[nt][2 * h + e] - dlt[h]) : 0.f;  // dS
         if (ok && irow[h] < N)  // slot d of query i: the key i - d
           a.pds[(static_cast<size_t>(bh) * N + irow[h]) * a.pds_stride + dist] = make_float2(p, S[nt][2 * h + e]);
       }

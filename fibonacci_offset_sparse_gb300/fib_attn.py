@@ -31,6 +31,7 @@ EXPORTS = [
     "fib_attn_fwd_prepare_kv", "fib_attn_fwd_attend", "fib_attn_bwd_workspace_size", "fib_attn_bwd",
     "fib_attn_debug_indices", "fib_attn_last_device_status", "fib_attn_plan_set_debug",
     "fib_attn_bwd_noalloc", "fib_attn_decode", "fib_attn_dense_fwd_workspace_size", "fib_attn_dense_fwd",
+    "fib_attn_debug_fill_shared",
 ]
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -60,6 +61,7 @@ _SIGS = {
                           _vp, _vp, ctypes.c_size_t, _vp]),
     "fib_attn_debug_indices": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "fib_attn_last_device_status": (_i, [_vp]),
+    "fib_attn_debug_fill_shared": (_i, [ctypes.c_uint32, _vp]),
     "fib_attn_plan_set_debug": (_i, [_vp, _i, ctypes.c_longlong]),
     "fib_attn_decode": (_i, [_vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "fib_attn_dense_fwd_workspace_size": (ctypes.c_size_t, [_vp, _i, _i, _i, _i]),
@@ -349,6 +351,12 @@ def fib_attn_plan_set_debug(plan: Plan, skip_first_rung_copy: bool, wait_ns: int
     flags = (FIB_DEBUG_SKIP_COPY if skip_first_rung_copy else 0) | \
         (FIB_DEBUG_CORRUPT_TABLE if corrupt_table else 0)
     _check("fib_attn_plan_set_debug", lib().fib_attn_plan_set_debug(plan.handle, flags, int(wait_ns)))
+
+
+def fib_attn_debug_fill_shared(pattern: int, stream=None):
+    """Test hook: fill every SM's shared memory with a 32-bit pattern (stale contents for the
+    kernels launched next)."""
+    _check("fib_attn_debug_fill_shared", lib().fib_attn_debug_fill_shared(int(pattern) & 0xffffffff, _stream(stream)))
 
 
 def fib_attn_last_device_status(plan: Plan) -> int:

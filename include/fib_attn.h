@@ -281,6 +281,13 @@ int fib_attn_debug_indices(fib_attn_plan_t p, int layer, int N, int i_begin, int
  * launch.  FIB_ERR_INVALID_ARG on a null plan, an unknown flag or wait_ns out of range.   */
 int fib_attn_plan_set_debug(fib_attn_plan_t p, int debug_flags, long long wait_ns);
 
+/* Test hook (no counterpart in the paper): fills the shared memory of every SM of the current
+ * device with the 32-bit `pattern` (one kernel taking each SM's whole shared memory), so that
+ * a test can check that no kernel lets stale shared memory reach its outputs (a pattern of
+ * 0x7fc00000 is a float NaN).  Enqueued on `stream`; allocates nothing.  FIB_ERR_CUDA on a
+ * failed launch.                                                                       */
+int fib_attn_debug_fill_shared(uint32_t pattern, void* stream);
+
 /* Synchronises the plan's device, then returns and clears the device status word (no
  * counterpart in the paper): FIB_OK, FIB_ERR_TIMEOUT (a bounded wait gave up),
  * FIB_ERR_DEVICE_ASSERT (the tensor-core forward's check of its rung table: every rung

@@ -632,3 +632,40 @@ def test_values_beyond_the_float16_limit_record_a_range_error(which):
                              oracle.fibonacci_base(), W, "mask")
     _check_o(o, O_ref, "bf16", "after range error")
     plan.close()
+
+
+# ------------------------------------------------------------------ stale shared memory
+@pytest.mark.parametrize("mode", ["mask", "interp"])
+@pytest.mark.parametrize("pattern", [0x7FC00000, 0x7C007C00])  # a float32 NaN; float16 infinities
+def test_stale_shared_memory_never_reaches_the_outputs(mode, pattern):
+    """Every SM's shared memory is filled with a NaN / infinity pattern before each call, so
+    that rows a kernel stages but does not copy (before position 0, after a ragged last row)
+    hold it; the bf16 forward, backward and dense kernels must still match the oracle."""
+    B, H, N, W, alpha = 2, 2, 333, 12, 1.2345
+    plan = _plan("fib", [alpha], W, N, mode)
+    q, k, v = inputs.qkv(B, H, N, 64, 540, 0, "bf16")
+    dO = inputs.upstream_grad(B, H, N, 64, 540, 0, "bf16")
+    qc, kc, vc, dOc = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+    fa.fib_attn_debug_fill_shared(pattern)
+    o, lse = fa.fib_attn_fwd(plan, 0, qc, kc, vc)
+    fa.fib_attn_debug_fill_shared(pattern)
+    dq, dk, dv, da = fa.fib_attn_bwd(plan, 0, qc, kc, vc, o, lse, dOc)
+    torch.cuda.synchronize()
+    assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+    qf, kf, vf, gf = (inputs.as_f64(x) for x in (q, k, v, dO))
+    O_ref, lse_ref = oracle.attend(qf, kf, vf, alpha, oracle.fibonacci_base(), W, mode)
+    _check_o(o, O_ref, "bf16", f"stale smem {mode}")
+    _check_lse(lse, lse_ref, "bf16", f"stale smem {mode}")
+    rq, rk, rv, ra, rss = _oracle_bwd(qf, kf, vf, gf, alpha, oracle.fibonacci_base(), W, mode)
+    for name, g, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        e = _rel_l2(g.double().cpu().numpy(), r)
+        assert e <= REL_L2, f"stale smem {mode} {name} rel-L2 {e:.3e}"
+    if mode == "interp":
+        _check_dalpha(da, ra, rss, f"stale smem {mode}")
+    fa.fib_attn_debug_fill_shared(pattern)
+    od, lsed = fa.fib_attn_dense_fwd(plan, qc, kc, vc)
+    torch.cuda.synchronize()
+    Od_ref, lsed_ref = oracle.attend(qf, kf, vf, 1.0, oracle.fibonacci_base(), N, "mask")
+    _check_o(od, Od_ref, "bf16", "stale smem dense")
+    _check_lse(lsed, lsed_ref, "bf16", "stale smem dense")
+    plan.close()
