@@ -58,7 +58,8 @@ struct BtcArgs {
   float* partials;
   int n_partials;   // CTAs of bwd_q_kernel
   float* dalpha;    // written by bwd_kv_kernel's CTA 0: the fixed-order sum of the partials
-  float2* pds;      // (P, dS) of every attended (query, key slot): [B*H*N][pds_stride]
+  float2* pds;      // (P, dS) of every attended (query, key slot): [B*H][pds_stride][N], slot-major
+                    // (a rung's slot of consecutive queries is contiguous: coalesced in both kernels)
   int pds_stride;   // W + rungs of the layer table
   const float2* rope_lo;
   const float2* rope_hi;
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
         const float p = ok ? exp2f(S[nt][2 * h + e] - lse2[h]) : 0.f;
         S[nt][2 * h + e] = ok ? p * (D[nt][2 * h + e] - dlt[h]) : 0.f;  // dS
         if (ok && irow[h] < N)  // slot d of query i: the key i - d
-          a.pds[(static_cast<size_t>(bh) * N + irow[h]) * a.pds_stride + dist] = make_float2(p, S[nt][2 * h + e]);
+          a.pds[(static_cast<size_t>(bh) * a.pds_stride + dist) * N + irow[h]] = make_float2(p, S[nt][2 * h + e]);
       }
 #pragma unroll
   for (int s2 = 0; s2 < 2; ++s2) {
@@ -467,7 +468,7 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
         const float P = ok[h] ? exp2f(s - lse2[h]) : 0.f;
         ds[h] = P * (dpp - dlt[h]);
         if (ok[h] && t == 0)  // slot W + r of query i (blended P and dS of the rung key)
-          a.pds[(static_cast<size_t>(bh) * N + irow[h]) * a.pds_stride + c] = make_float2(P, ds[h]);
+          a.pds[(static_cast<size_t>(bh) * a.pds_stride + c) * N + irow[h]] = make_float2(P, ds[h]);
         if (MODE == 1) {
           // dl/dw = dS (s1 - s0) + P (dO.v1 - dO.v0) (natural units), dw/dalpha = f; the
           // partner row i-lo-1 must exist (it only does not when w = 0 and i = lo)
@@ -624,7 +625,6 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
   // wait for it, and its writes, before the first load of them
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const float2* pds = a.pds + static_cast<size_t>(bh) * N * a.pds_stride;
-  const int stride = a.pds_stride;
 
   float dK[8][4], dV[8][4];  // natural accumulator layout, rows = keys g, g+8
 #pragma unroll
@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
           const int c = 8 * nt + 2 * t + e;
           const int d = c - (g + 8 * h);
           const bool ok = d >= 0 && d < W && k0 + c < N && k0 + g + 8 * h < N;
-          const float2 v = ok ? __ldg(pds + static_cast<size_t>(k0 + c) * stride + d) : make_float2(0.f, 0.f);
+          const float2 v = ok ? __ldg(pds + static_cast<size_t>(d) * N + (k0 + c)) : make_float2(0.f, 0.f);
           D[nt][2 * h + e] = v.x;
           S[nt][2 * h + e] = v.y;
         }
@@ -693,7 +693,7 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
       for (int h = 0; h < 2; ++h) {
         const int i = k0 + g + 8 * h + lo + role;
         const bool ok = (role == 0 || MODE == 1) && k0 + g + 8 * h <= j_last && i < N && i >= need;
-        v[role][h] = ok ? __ldg(pds + static_cast<size_t>(i) * stride + c) : make_float2(0.f, 0.f);
+        v[role][h] = ok ? __ldg(pds + static_cast<size_t>(c) * N + i) : make_float2(0.f, 0.f);
       }
   };
   float2 vn[2][2];
