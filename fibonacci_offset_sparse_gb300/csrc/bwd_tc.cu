@@ -38,6 +38,7 @@ constexpr int kBCons = 32 * kBWarps;
 constexpr int kBThreadsT = kBCons + 32;    // + one producer warp
 constexpr int kBSlots = 3;
 constexpr int kKvQRows = kBTileT + 16;     // query rows a kv stage holds (window block: 80)
+constexpr int kBWinMax = 16;               // widest window of the tensor-core backward
 
 struct BtcArgs {
   LayerTable t;
@@ -317,6 +318,7 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
   release_stage(0);
 
   // ---- window: S = Q's K'^T, dP = dO' V'^T over keys [q0-16, q0+16); dq' += dS K'
+  float2* wst = reinterpret_cast<float2*>(ring + kBSlots * a.slot_bytes) + warp * 16 * kBWinMax;  // [slot][row]
   float acc[8][4];  // dq' in the natural accumulator layout
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
@@ -354,9 +356,15 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
         // so that no stale NaN or infinity can reach dS through a product with p = 0
         const float p = ok ? exp2f(S[nt][2 * h + e] - lse2[h]) : 0.f;
         S[nt][2 * h + e] = ok ? p * (D[nt][2 * h + e] - dlt[h]) : 0.f;  // dS
-        if (ok && irow[h] < N)  // slot d of query i: the key i - d
-          a.pds[(static_cast<size_t>(bh) * a.pds_stride + dist) * N + irow[h]] = make_float2(p, S[nt][2 * h + e]);
+        // slot d of query row g + 8h (the key i - d), staged so that the warp writes each slot's
+        // 16 queries as one contiguous run below; every (slot < W, row) is one element here
+        if (dist >= 0 && dist < W) wst[dist * 16 + g + 8 * h] = make_float2(p, S[nt][2 * h + e]);
       }
+  __syncwarp();
+  for (int d0 = 0; d0 < W; d0 += 2) {  // two slots a store: lanes 0-15 slot d0, 16-31 slot d0 + 1
+    const int d = d0 + (lane >> 4), r = lane & 15;
+    if (d < W && q0 + r < N) a.pds[(static_cast<size_t>(bh) * a.pds_stride + d) * N + q0 + r] = wst[d * 16 + r];
+  }
 #pragma unroll
   for (int s2 = 0; s2 < 2; ++s2) {
     const uint32_t pa0 = pack_h2(S[2 * s2][0], S[2 * s2][1]);
@@ -753,7 +761,7 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
 }
 
 // ------------------------------------------------------------------ launch
-bool bwd_tc_supported(const LayerTable& t) { return t.W <= 16; }
+bool bwd_tc_supported(const LayerTable& t) { return t.W <= kBWinMax; }
 
 size_t bwd_tc_workspace_bytes(int B, int H, int N, int W) {
   const size_t rows = static_cast<size_t>(B) * H * N;
@@ -809,7 +817,7 @@ cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   a.slot_bytes = 2 * a.slab_rows * kRowBytes;
   {
     // a programmatic dependent of the preparation grid: the CTAs' prologue overlaps its tail
-    const int smem = kBSlots * a.slot_bytes;
+    const int smem = kBSlots * a.slot_bytes + kBWarps * 16 * kBWinMax * static_cast<int>(sizeof(float2));
     void (*kern)(BtcArgs) = t.mode == 0 ? bwd_q_kernel<0> : bwd_q_kernel<1>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
