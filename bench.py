@@ -95,12 +95,34 @@ def read_peaks():
         return HBM_FALLBACK_GBS, "fallback"
 
 
-def kernel_source_hash():
+def source_hash(files):
     h = hashlib.sha256()
-    for fn in ("common.cuh", "tc_common.cuh", "fwd.cu", "fwd_tc.cu"):
+    for fn in files:
         with open(os.path.join(ROOT, "fibonacci_offset_sparse_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def kernel_source_hash():
+    """Hash of the forward kernels' sources (a profile summary names the one it was taken on)."""
+    return source_hash(("common.cuh", "tc_common.cuh", "fwd.cu", "fwd_tc.cu"))
+
+
+def backward_source_hash():
+    """Hash of the tensor-core backward's sources."""
+    return source_hash(("common.cuh", "tc_common.cuh", "bwd_tc.cu"))
+
+
+def profile_fields(name):
+    """The `- key: value` fields of a committed profile summary (empty when it is absent)."""
+    p = os.path.join(ROOT, "profiles", name)
+    vals = {}
+    if os.path.exists(p):
+        for line in open(p):
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip()
+    return vals
 
 
 def ncu_traffic(workload):
@@ -108,18 +130,23 @@ def ncu_traffic(workload):
     {"layer": steady-state bytes of both kernels of a layer inside the stack, "attend": the
     attention kernel's bytes in that capture}, or None when the summary is absent or was taken
     on a different kernel source."""
-    p = os.path.join(ROOT, "profiles", f"fwd_{workload}.md")
-    if not os.path.exists(p):
-        return None
-    vals = {}
-    for line in open(p):
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip()
+    vals = profile_fields(f"fwd_{workload}.md")
     if vals.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
     try:
         return {"layer": float(vals["layer_dram_bytes_steady"]), "attend": float(vals["attend_dram_bytes_steady"])}
+    except Exception:
+        return None
+
+
+def ncu_traffic_bwd(workload):
+    """Steady-state DRAM bytes of one backward layer (its three kernels) from the committed ncu
+    summary, or None when it is absent or was taken on a different kernel source."""
+    vals = profile_fields(f"bwd_{workload}.md")
+    if vals.get("kernel_source_sha256_16") != backward_source_hash():
+        return None
+    try:
+        return float(vals["layer_dram_bytes_steady"])
     except Exception:
         return None
 
@@ -397,8 +424,10 @@ def time_backward(w, steps, warmup, device):
            for l in range(w["L"])]
     grads = [tuple(torch.empty_like(d[0]) for _ in range(3)) for d in dev]
     dal = [torch.empty(1, dtype=torch.float32, device=device) for _ in dev]
+    # one backward workspace for the stack: the prepared rows and (P, dS) pairs are scratch
+    # that each layer's backward consumes before the next layer's starts, as in a model
     need = fa.fib_attn_bwd_workspace_size(plan, w["B"], w["H"], w["N"])
-    bws = [torch.empty(need, dtype=torch.uint8, device=device) for _ in dev]
+    bws = [torch.empty(need, dtype=torch.uint8, device=device)] * len(dev)
 
     def bwd_stack():
         for l, (q, k, v) in enumerate(dev):
@@ -653,7 +682,8 @@ def main():
                             "ms_per_step": rb["ms_per_step"], "us_per_layer": rb["us_per_layer"],
                             "compulsory_bytes_per_layer": bb,
                             "achieved_gbs": bb / (rb["us_per_layer"] * 1e-6) / 1e9,
-                            "frac": bb / (rb["us_per_layer"] * 1e-6) / 1e9 / peak}
+                            "frac": bb / (rb["us_per_layer"] * 1e-6) / 1e9 / peak,
+                            "traffic": ncu_traffic_bwd(BACKWARD)}
     dense = {}
     for name in [args.workload] + (SECONDARY if args.workload == DEFAULT and not args.no_secondary else []):
         ws = WORKLOADS[name]

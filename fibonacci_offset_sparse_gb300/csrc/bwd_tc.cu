@@ -39,6 +39,7 @@ constexpr int kBThreadsT = kBCons + 32;    // + one producer warp
 constexpr int kBSlots = 3;
 constexpr int kKvQRows = kBTileT + 16;     // query rows a kv stage holds (window block: 80)
 constexpr int kBWinMax = 16;               // widest window of the tensor-core backward
+constexpr int kKvPdsBytes = 68 * 8;        // a kv rung stage's (P, dS) run: 65 queries, rounded
 
 struct BtcArgs {
   LayerTable t;
@@ -535,7 +536,9 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_q_kernel(BtcArgs a) {
 
 // ------------------------------------------------------------------ key-owned: dk, dv
 // Stage 0 brings the window block's Q's and dO' rows [j0, j0+80), stage 1+r the query slab
-// of rung r: rows [j0+lo, j0+lo+65).  P and dS come from bwd_q_kernel.
+// of rung r: rows [j0+lo, j0+lo+65), and those queries' (P, dS) of the rung's slot (one
+// contiguous run in the slot-major array, copied from the even element at or before it, so
+// that the copy starts and ends on 16 bytes).  P and dS come from bwd_q_kernel.
 template <int MODE>
 __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
   __shared__ KeySmem ks;
@@ -600,11 +603,22 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
       const int qrows = n == 0 ? kKvQRows : kBTileT + 1;
       const int q1 = min(qfirst + qrows, N);
       const uint32_t qbytes = q1 > qfirst ? static_cast<uint32_t>(q1 - qfirst) * kRowBytes : 0u;
-      mbar_arrive_tx(&full_bar[slot], 2 * qbytes);
+      uint32_t pbytes = 0;
+      size_t p0 = 0;
+      if (n > 0 && qbytes) {
+        // P and dS are written by the dQ grid launched just before: wait for it (stage 0
+        // holds only rows of the preparation, which completed before this grid launched)
+        if (n == 1) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        const size_t e0 = (static_cast<size_t>(bh) * a.pds_stride + W + n - 1) * N + qfirst;
+        p0 = e0 & ~static_cast<size_t>(1);
+        pbytes = static_cast<uint32_t>(((e0 + (q1 - qfirst) + 1) & ~static_cast<size_t>(1)) - p0) * sizeof(float2);
+      }
+      mbar_arrive_tx(&full_bar[slot], 2 * qbytes + pbytes);
       if (qbytes) {
         bulk_g2s(dst, a.qs + base + static_cast<size_t>(qfirst) * kD, qbytes, &full_bar[slot]);
         bulk_g2s(dst + kQ2, a.dos + base + static_cast<size_t>(qfirst) * kD, qbytes, &full_bar[slot]);
       }
+      if (pbytes) bulk_g2s(dst + 2 * kQ2, a.pds + p0, pbytes, &full_bar[slot]);
       last_n[slot] = n;
     }
 #pragma unroll
@@ -689,38 +703,31 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
   // of query i: i - (j0 + lo).  dk' += diag(wt dS) Q's[slab], dv += diag(wt P) dO'[slab].
   const float sel_lo = (t == (g >> 1) && !(g & 1)) ? 1.f : 0.f;
   const float sel_hi = (t == (g >> 1) && (g & 1)) ? 1.f : 0.f;
-  // stored (P, dS) of the query of key k0 + g + 8h for each role: loaded one rung ahead, so
-  // that their latency overlaps the previous rung's products
-  auto load_pds = [&](int r, float2 (&v)[2][2]) {
-    const int c = W + r;
-    const int lo = ks.lo[c];
-    const int need = ks.need[c];
-#pragma unroll
-    for (int role = 0; role < 2; ++role)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int i = k0 + g + 8 * h + lo + role;
-        const bool ok = (role == 0 || MODE == 1) && k0 + g + 8 * h <= j_last && i < N && i >= need;
-        v[role][h] = ok ? __ldg(pds + static_cast<size_t>(c) * N + i) : make_float2(0.f, 0.f);
-      }
-  };
-  float2 vn[2][2];
-  if (nrk > 0) load_pds(0, vn);
   for (int r = 0; r < nrk; ++r) {
     const int n = 1 + r;
     const int c = W + r;
     const int lo = ks.lo[c];
+    const int need = ks.need[c];
     const float w = MODE == 1 ? ks.w[c] : 0.f;
     const int qfirst = j0 + lo;
     const int xlast = min(qfirst + kBTileT, N - 1) - qfirst;  // last copied slab row
+    // the stage's (P, dS) run starts one element early when the query's is odd
+    const int par = static_cast<int>(((static_cast<size_t>(bh) * a.pds_stride + c) * N + qfirst) & 1);
+    wait_stage(n);
+    const unsigned char* qst = slot_of(n);
+    const float2* sp = reinterpret_cast<const float2*>(qst + 2 * kQ2) + par;
+    // stored (P, dS) of the query i of key k0 + g + 8h for each role; entries of queries
+    // before the rung's first attending one or past N are not the dQ grid's: never used
     float2 v[2][2];  // [role][h]
 #pragma unroll
     for (int role = 0; role < 2; ++role)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) v[role][h] = vn[role][h];
-    if (r + 1 < nrk) load_pds(r + 1, vn);
-    wait_stage(n);
-    const unsigned char* qst = slot_of(n);
+      for (int h = 0; h < 2; ++h) {
+        const int x = 16 * warp + g + 8 * h + role;  // slab row of query i = qfirst + x
+        const int i = qfirst + x;
+        const bool ok = (role == 0 || MODE == 1) && k0 + g + 8 * h <= j_last && i < N && i >= need;
+        v[role][h] = ok ? sp[x] : make_float2(0.f, 0.f);
+      }
 #pragma unroll
     for (int role = 0; role < (MODE == 1 ? 2 : 1); ++role) {
       if (role == 1 && !(w > 0.f)) continue;  // uniform: weight 0
@@ -768,7 +775,7 @@ size_t bwd_tc_workspace_bytes(int B, int H, int N, int W) {
   const size_t tiles = (static_cast<size_t>(N) + kBTileT - 1) / kBTileT * B * H;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   return 4 * up(rows * kRowBytes) + up(rows * sizeof(float)) + up(tiles * sizeof(float)) +
-         up(rows * (W + kMaxR) * sizeof(float2));
+         up(rows * (W + kMaxR) * sizeof(float2) + 16);  // + the dK/dV copies' rounding
 }
 
 cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k, const void* v,
@@ -840,7 +847,7 @@ cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   // only at their end, after each of their threads waited for the preparation grid, so that
   // grid has completed before this one launches.
   a.slab_rows = kKvQRows;
-  a.slot_bytes = 2 * kKvQRows * kRowBytes;
+  a.slot_bytes = 2 * kKvQRows * kRowBytes + kKvPdsBytes;
   a.n_partials = static_cast<int>(blocks);
   a.dalpha = dalpha;
   {
