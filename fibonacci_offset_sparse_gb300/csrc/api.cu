@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <set>
 #include <vector>
@@ -35,7 +36,7 @@ size_t bwd_tc_workspace_bytes(int B, int H, int N, int W);
 cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k, const void* v,
                           const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
                           float* dalpha, void* ws, const float2* lo_tab, const float2* hi_tab, int* status,
-                          unsigned long long wait_ns, cudaStream_t stream);
+                          unsigned long long wait_ns, cudaStream_t stream, const BwdStreams& side);
 cudaError_t launch_bwd(const LayerTable& t, int B, int H, int N, int dtype, const void* q,
                        const void* k, const void* v, const void* o, const float* lse,
                        const void* dO, void* dq, void* dk, void* dv, float* dalpha, void* ws,
@@ -77,11 +78,24 @@ struct fib_attn_plan_s {
   unsigned long long wait_ns = 1000000000ULL;  // bound of every device-side wait (1 s)
   int skip_first_rung_copy = 0;                // test hooks, see fib_attn_plan_set_debug
   int corrupt_rung_table = 0;
+  BwdStreams side;                             // the bf16 backward's second-half stream
+  std::mutex side_mu;                          // one backward at a time forks onto it
 };
 
 namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Frees what a plan holds on the device (each handle may be null).
+void release_device_state(fib_attn_plan_s* p) {
+  cudaFree(p->d_lo);
+  cudaFree(p->d_hi);
+  cudaFree(p->d_status);
+  if (p->side.join) cudaEventDestroy(p->side.join);
+  if (p->side.first_q_done) cudaEventDestroy(p->side.first_q_done);
+  if (p->side.fork) cudaEventDestroy(p->side.fork);
+  if (p->side.stream) cudaStreamDestroy(p->side.stream);
+}
 
 std::vector<int32_t> plan_base(const fib_attn_plan_s* p, int N) {
   if (p->base_kind == FIB_BASE_FIBONACCI) return fibonacci_base(987);
@@ -289,10 +303,12 @@ int fib_attn_plan_create(fib_attn_plan_t* out, int base_kind, const int32_t* cus
   if (e == cudaSuccess) e = cudaMemcpy(p->d_lo, lo.data(), lo.size() * sizeof(float), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(p->d_hi, hi.data(), hi.size() * sizeof(float), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->side.stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->side.fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->side.first_q_done, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->side.join, cudaEventDisableTiming);
   if (e != cudaSuccess) {
-    cudaFree(p->d_lo);
-    cudaFree(p->d_hi);
-    cudaFree(p->d_status);
+    release_device_state(p);
     delete p;
     return cuda_status(e);
   }
@@ -306,9 +322,7 @@ int fib_attn_plan_destroy(fib_attn_plan_t p) {
   cudaGetDevice(&prev);
   if (p->device >= 0) cudaSetDevice(p->device);
   cudaDeviceSynchronize();
-  cudaFree(p->d_lo);
-  cudaFree(p->d_hi);
-  cudaFree(p->d_status);
+  release_device_state(p);
   if (prev >= 0) cudaSetDevice(prev);
   delete p;
   return FIB_OK;
@@ -480,9 +494,11 @@ int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, c
   if (st != FIB_OK) return st;
   // bf16 with a window of at most 16 keys: prepared rows + tensor-core kernels (bwd_tc.cu);
   // otherwise the CUDA-core kernels (bwd.cu), which also serve float32
-  if (dtype == FIB_DTYPE_BF16 && bwd_tc_supported(t))
+  if (dtype == FIB_DTYPE_BF16 && bwd_tc_supported(t)) {
+    std::lock_guard<std::mutex> lock(p->side_mu);
     return cuda_status(launch_bwd_tc(t, B, H, N, q, k, v, o, lse, dO, dq, dk, dv, dalpha, workspace, p->d_lo,
-                                     p->d_hi, p->d_status, p->wait_ns, static_cast<cudaStream_t>(stream)));
+                                     p->d_hi, p->d_status, p->wait_ns, static_cast<cudaStream_t>(stream), p->side));
+  }
   return cuda_status(launch_bwd(t, B, H, N, dtype, q, k, v, o, lse, dO, dq, dk, dv, dalpha,
                                 workspace, p->d_lo, p->d_hi, static_cast<cudaStream_t>(stream)));
 }

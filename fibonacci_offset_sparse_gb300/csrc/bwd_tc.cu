@@ -577,8 +577,8 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
 
   // ===================================================================== producer
   if (warp == kBWarps) {
-    if (blockIdx.x == 0) {
-      // dalpha of the layer: the dQ grid's partials, summed in a fixed order (lane l takes
+    if (blockIdx.x == 0 && a.dalpha != nullptr) {
+      // dalpha of the layer: the dQ grids' partials, summed in a fixed order (lane l takes
       // partials l, l+32, ... in turn, then a fixed shuffle tree)
       asm volatile("griddepcontrol.wait;\n" ::: "memory");
       float acc = 0.f;
@@ -770,56 +770,72 @@ __global__ void __launch_bounds__(kBThreadsT, 3) bwd_kv_kernel(BtcArgs a) {
 // ------------------------------------------------------------------ launch
 bool bwd_tc_supported(const LayerTable& t) { return t.W <= kBWinMax; }
 
+namespace {
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+// The scratch of one half of the (b, h) rows: Q's, dO', K', V' rows, Delta, (P, dS) pairs.
+size_t half_bytes(long long bh, int N, int W) {
+  const size_t rows = static_cast<size_t>(bh) * N;
+  return 4 * up256(rows * kRowBytes) + up256(rows * sizeof(float)) +
+         up256(rows * (W + kMaxR) * sizeof(float2) + 16);  // + the dK/dV copies' rounding
+}
+// The rows of the first half: the (b, h) rows split in two when there are two or more.
+long long first_half(long long bh) { return bh >= 2 ? bh / 2 : bh; }
+}  // namespace
+
 size_t bwd_tc_workspace_bytes(int B, int H, int N, int W) {
-  const size_t rows = static_cast<size_t>(B) * H * N;
-  const size_t tiles = (static_cast<size_t>(N) + kBTileT - 1) / kBTileT * B * H;
-  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  return 4 * up(rows * kRowBytes) + up(rows * sizeof(float)) + up(tiles * sizeof(float)) +
-         up(rows * (W + kMaxR) * sizeof(float2) + 16);  // + the dK/dV copies' rounding
+  const long long bh = static_cast<long long>(B) * H;
+  const size_t tiles = (static_cast<size_t>(N) + kBTileT - 1) / kBTileT * bh;
+  const long long bh0 = first_half(bh);
+  return up256(tiles * sizeof(float)) + half_bytes(bh0, N, W) + (bh > bh0 ? half_bytes(bh - bh0, N, W) : 0);
 }
 
-cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k, const void* v,
-                          const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                          float* dalpha, void* ws, const float2* lo_tab, const float2* hi_tab, int* status,
-                          unsigned long long wait_ns, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(B) * H * N;
-  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  unsigned char* w = static_cast<unsigned char*>(ws);
-  const size_t arr = up(static_cast<size_t>(rows) * kRowBytes);
+namespace {
+// The three launches of the (b, h) rows [off, off + n) on one stream.  The dQ grid writes its
+// CTAs' dalpha partials at partials + n_before; the dK/dV grid sums partials[0 .. n_sum) into
+// dalpha when dalpha is not null.  record_after_q, when given, is recorded between the dQ and
+// the dK/dV launch (it marks the end of the dQ grid for the other half); wait_before_kv, when
+// given, is an event the dK/dV launch waits for first (the other half's dQ grid, whose
+// partials it sums too).
+cudaError_t launch_half(const LayerTable& t, long long off, long long n, int N, const void* q, const void* k,
+                        const void* v, const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                        float* partials, long long n_before, long long n_sum, float* dalpha, unsigned char* w,
+                        const float2* lo_tab, const float2* hi_tab, int* status, unsigned long long wait_ns,
+                        cudaEvent_t record_after_q, cudaEvent_t wait_before_kv, cudaStream_t stream) {
+  const long long rows = n * N;
+  const size_t eo = static_cast<size_t>(off) * N * kD;  // element offset of the half's rows
+  auto bf = [&](const void* x) { return static_cast<const __nv_bfloat16*>(x) + eo; };
+  auto bfo = [&](void* x) { return static_cast<__nv_bfloat16*>(x) + eo; };
+  const size_t arr = up256(static_cast<size_t>(rows) * kRowBytes);
   BtcArgs a;
   a.t = t;
   a.N = N;
   a.tiles = (N + kBTileT - 1) / kBTileT;
-  a.bh = B * H;
+  a.bh = static_cast<int>(n);
   a.qs = reinterpret_cast<const __half*>(w);
   a.dos = reinterpret_cast<const __half*>(w + arr);
   a.kp = reinterpret_cast<const __half*>(w + 2 * arr);
   a.vp = reinterpret_cast<const __half*>(w + 3 * arr);
   float* delta = reinterpret_cast<float*>(w + 4 * arr);
   a.delta = delta;
-  const size_t tiles_all = static_cast<size_t>(a.tiles) * B * H;
-  a.partials = reinterpret_cast<float*>(w + 4 * arr + up(static_cast<size_t>(rows) * sizeof(float)));
-  a.pds = reinterpret_cast<float2*>(w + 4 * arr + up(static_cast<size_t>(rows) * sizeof(float)) +
-                                    up(tiles_all * sizeof(float)));
+  a.pds = reinterpret_cast<float2*>(w + 4 * arr + up256(static_cast<size_t>(rows) * sizeof(float)));
   a.pds_stride = t.W + t.n;  // the kernels keep at most t.n rungs
-  a.lse = lse;
-  a.dq = static_cast<__nv_bfloat16*>(dq);
-  a.dk = static_cast<__nv_bfloat16*>(dk);
-  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.lse = lse + static_cast<size_t>(off) * N;
+  a.dq = bfo(dq);
+  a.dk = bfo(dk);
+  a.dv = bfo(dv);
   a.rope_lo = lo_tab;
   a.rope_hi = hi_tab;
   a.status = status;
   a.wait_ns = wait_ns;
-  const long long blocks = static_cast<long long>(a.tiles) * B * H;
+  const long long blocks = static_cast<long long>(a.tiles) * n;
   const long long prep_blocks = (rows * 4 + 255) / 256;
   if (blocks > 0x7fffffffLL || prep_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   bwd_prep_kernel<<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), const_cast<__half*>(a.qs),
-      const_cast<__half*>(a.kp), const_cast<__half*>(a.vp), const_cast<__half*>(a.dos), delta, lo_tab, hi_tab, N, rows,
-      kLog2e / 8.0f, status);
+      bf(q), bf(k), bf(v), bf(o), bf(dO), const_cast<__half*>(a.qs), const_cast<__half*>(a.kp),
+      const_cast<__half*>(a.vp), const_cast<__half*>(a.dos), delta, lo_tab, hi_tab, N, rows, kLog2e / 8.0f, status);
   cudaError_t e;
   // query-owned: dq and the dalpha partials
+  a.partials = partials + n_before;
   a.slab_rows = t.mode == 1 ? kBTileT + 8 : kBTileT;
   a.slot_bytes = 2 * a.slab_rows * kRowBytes;
   {
@@ -841,6 +857,14 @@ cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* 
     e = cudaLaunchKernelEx(&cfg, kern, a);
     if (e != cudaSuccess) return e;
   }
+  if (record_after_q != nullptr) {
+    e = cudaEventRecord(record_after_q, stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (wait_before_kv != nullptr) {
+    e = cudaStreamWaitEvent(stream, wait_before_kv, 0);
+    if (e != cudaSuccess) return e;
+  }
   // key-owned: dk, dv, and dalpha (CTA 0), launched as a programmatic dependent of the dQ
   // grid: its prologue and first copies (of rows the preparation wrote) overlap that grid's
   // tail; it waits for the grid before it reads P, dS and the partials.  The dQ CTAs signal
@@ -848,7 +872,8 @@ cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   // grid has completed before this one launches.
   a.slab_rows = kKvQRows;
   a.slot_bytes = 2 * kKvQRows * kRowBytes + kKvPdsBytes;
-  a.n_partials = static_cast<int>(blocks);
+  a.partials = partials;
+  a.n_partials = static_cast<int>(n_sum);
   a.dalpha = dalpha;
   {
     const int smem = kBSlots * a.slot_bytes;
@@ -869,6 +894,39 @@ cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* 
     if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k, const void* v,
+                          const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                          float* dalpha, void* ws, const float2* lo_tab, const float2* hi_tab, int* status,
+                          unsigned long long wait_ns, cudaStream_t stream, const BwdStreams& side) {
+  // The (b, h) rows run as two halves, the second on the side stream (forked from and joined
+  // back to `stream` with events): each half's grids then fill the SMs that the other half's
+  // last, partly filled wave of CTAs leaves idle.  The first half's dK/dV grid leaves dalpha
+  // alone; the second half's waits for the first half's dQ grid too and sums every partial
+  // of both, in one fixed order.
+  const long long bh = static_cast<long long>(B) * H;
+  const long long bh0 = first_half(bh);
+  const long long tiles = (N + kBTileT - 1) / kBTileT;
+  unsigned char* w = static_cast<unsigned char*>(ws);
+  float* partials = reinterpret_cast<float*>(w);
+  unsigned char* w0 = w + up256(static_cast<size_t>(tiles * bh) * sizeof(float));
+  unsigned char* w1 = w0 + half_bytes(bh0, N, t.W);
+  if (bh == bh0)
+    return launch_half(t, 0, bh, N, q, k, v, o, lse, dO, dq, dk, dv, partials, 0, tiles * bh, dalpha, w0, lo_tab,
+                       hi_tab, status, wait_ns, nullptr, nullptr, stream);
+  cudaError_t e = cudaEventRecord(side.fork, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.fork, 0);
+  if (e == cudaSuccess)
+    e = launch_half(t, 0, bh0, N, q, k, v, o, lse, dO, dq, dk, dv, partials, 0, 0, nullptr, w0, lo_tab, hi_tab,
+                    status, wait_ns, side.first_q_done, nullptr, stream);
+  if (e == cudaSuccess)
+    e = launch_half(t, bh0, bh - bh0, N, q, k, v, o, lse, dO, dq, dk, dv, partials, tiles * bh0, tiles * bh, dalpha,
+                    w1, lo_tab, hi_tab, status, wait_ns, nullptr, side.first_q_done, side.stream);
+  if (e == cudaSuccess) e = cudaEventRecord(side.join, side.stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, side.join, 0);
+  return e;
 }
 
 }  // namespace fibattn

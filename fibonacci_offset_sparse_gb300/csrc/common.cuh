@@ -36,6 +36,15 @@ struct LayerTable {
   int32_t f[kMaxR];
 };
 
+// The side stream and events onto which the bf16 backward forks the second half of its
+// (b, h) rows (owned by a plan, created with it).
+struct BwdStreams {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr;          // the caller's stream has reached the call
+  cudaEvent_t first_q_done = nullptr;  // the first half's dQ grid has completed
+  cudaEvent_t join = nullptr;          // the second half has completed
+};
+
 // Virtual keys of a layer, built in shared memory by the CTA prologue.
 struct KeySmem {
   int nv;              // window + rungs

@@ -224,6 +224,12 @@ int fib_attn_decode(fib_attn_plan_t p, int layer, int B, int H, int N, int pos, 
  * for both dtypes: for a plan with W <= 16 it is what the bf16 path needs (Q, K, V, dO
  * prepared once as float16 rows, B*H*N*512 bytes, plus Delta and the dalpha partials);
  * the float32 path uses only the first B*H*N*4 bytes and the partials.
+ * Streams: on the bf16 tensor-core path with B*H >= 2, the second half of the (b, h) rows
+ * runs on a stream the plan owns, forked from `stream` and joined back to it with events
+ * before the call returns (so that work enqueued on `stream` afterwards, and a stream
+ * capture of `stream`, see the whole backward); one plan's backward calls from several host
+ * threads take turns to enqueue, and their device work must not overlap (the same stream,
+ * or ordered by the caller).
  * Errors as fib_attn_fwd, plus FIB_ERR_INVALID_ARG for a short/misaligned workspace.  */
 size_t fib_attn_bwd_workspace_size(fib_attn_plan_t p, int B, int H, int N);
 int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
