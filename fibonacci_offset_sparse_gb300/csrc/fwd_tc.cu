@@ -94,58 +94,99 @@ struct TcArgs {
 };
 
 // ------------------------------------------------------------------ K', V' preparation
-// One thread per (row, quarter u): frequencies m = 8u .. 8u+7, i.e. chunks u (dims 8u..) and
-// u+4 (their rotate-half partners 32+8u..) of the K row, and the same two chunks of V.
-__global__ void __launch_bounds__(256) prep_kv_kernel(const __nv_bfloat16* __restrict__ k,
-                                                      const __nv_bfloat16* __restrict__ v,
-                                                      __half* __restrict__ kp, __half* __restrict__ vp,
-                                                      const float2* __restrict__ lo_tab,
-                                                      const float2* __restrict__ hi_tab, int N,
-                                                      long long rows, int* __restrict__ status) {
+// A warp prepares 32 consecutive rows: lane (j8 = lane/4, u = lane%4) handles rows
+// base + 8i + j8 (i < kPrepIters) and the frequencies m = 8u .. 8u+7, i.e. chunks u (dims
+// 8u..) and u+4 (their rotate-half partners 32+8u..) of the K row, and the same two chunks
+// of V.  Every load of the warp is issued first.  The RoPE factors e^{i p theta_m} of the
+// first row come from the factored tables; each later row of the lane sits 8 positions
+// further, so its factors are the previous ones times e^{i 8 theta_m} (one complex product
+// each, relative error ~1e-7 a step, far below the float16 rounding of K'), unless a new
+// sequence began in between (position < 8), where the tables are read again.  This keeps
+// the table reads at a few bytes a row instead of 128.
+constexpr int kPrepIters = 4;
+constexpr int kPrepThreads = 128;
+constexpr int kPrepRowsPerBlock = kPrepThreads / 4 * kPrepIters;  // 128
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kv_kernel(const __nv_bfloat16* __restrict__ k,
+                                                               const __nv_bfloat16* __restrict__ v,
+                                                               __half* __restrict__ kp, __half* __restrict__ vp,
+                                                               const float2* __restrict__ lo_tab,
+                                                               const float2* __restrict__ hi_tab, int N,
+                                                               long long rows, int* __restrict__ status) {
   // The dependent attention grid may launch at once: its CTAs take the SMs as this grid
   // drains and load and rotate their Q rows meanwhile; each waits for the whole of this grid
   // (griddepcontrol.wait) before it reads K'/V'.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  const long long gid = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
-  const long long row = gid >> 2;
-  if (row >= rows) return;
-  const int u = static_cast<int>(gid & 3);
-  const int p = static_cast<int>(row % N);
-  const uint4* k4 = reinterpret_cast<const uint4*>(k + row * kD);
-  const uint4* v4 = reinterpret_cast<const uint4*>(v + row * kD);
-  const uint4 ka = __ldcs(k4 + u), kb = __ldcs(k4 + u + 4), va = __ldcs(v4 + u), vb = __ldcs(v4 + u + 4);
+  const int lane = threadIdx.x & 31;
+  const int u = lane & 3, j8 = lane >> 2;
+  const long long base = static_cast<long long>(blockIdx.x) * kPrepRowsPerBlock + (threadIdx.x >> 5) * 32 + j8;
+  uint4 ka[kPrepIters], kb[kPrepIters], va[kPrepIters], vb[kPrepIters];
+#pragma unroll
+  for (int i = 0; i < kPrepIters; ++i) {
+    const long long row = base + 8 * i;
+    if (row < rows) {
+      const uint4* k4 = reinterpret_cast<const uint4*>(k + row * kD);
+      const uint4* v4 = reinterpret_cast<const uint4*>(v + row * kD);
+      ka[i] = __ldcs(k4 + u);
+      kb[i] = __ldcs(k4 + u + 4);
+      va[i] = __ldcs(v4 + u);
+      vb[i] = __ldcs(v4 + u + 4);
+    }
+  }
+  float2 step[8];  // e^{i 8 theta_m}: row 8 of the low table
+  {
+    const float4* s4 = reinterpret_cast<const float4*>(lo_tab + 8 * kFreq + 8 * u);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float4 x = __ldg(s4 + w);
+      step[2 * w] = make_float2(x.x, x.y);
+      step[2 * w + 1] = make_float2(x.z, x.w);
+    }
+  }
   float2 e[8];
-  rope_row(lo_tab, hi_tab, p, u, e);
-  const uint32_t xa[4] = {ka.x, ka.y, ka.z, ka.w}, xb[4] = {kb.x, kb.y, kb.z, kb.w};
-  uint32_t ya[4], yb[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    // (k_m, k_{m+32}) -> (k_m cos - k_{m+32} sin, k_m sin + k_{m+32} cos), m = 8u + 2c (+1)
-    const float k1x = bf_lo(xa[c]), k1y = bf_hi(xa[c]), k2x = bf_lo(xb[c]), k2y = bf_hi(xb[c]);
-    const float2 e0 = e[2 * c], e1 = e[2 * c + 1];
-    ya[c] = pack_h2(k1x * e0.x - k2x * e0.y, k1y * e1.x - k2y * e1.y);
-    yb[c] = pack_h2(k1x * e0.y + k2x * e0.x, k1y * e1.y + k2y * e1.x);
-  }
-  const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
-  uint32_t za[4], zb[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    za[c] = pack_h2(bf_lo(wa[c]), bf_hi(wa[c]));
-    zb[c] = pack_h2(bf_lo(wb[c]), bf_hi(wb[c]));
-  }
-  // A rotated key or a value beyond the float16 range (|x| > 65504) cannot be represented
-  // in the prepared rows: record it (the outputs of this call are then unspecified).
   uint32_t bad = 0;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) bad |= h2_nonfinite(ya[c]) | h2_nonfinite(yb[c]) | h2_nonfinite(za[c]) | h2_nonfinite(zb[c]);
+  for (int i = 0; i < kPrepIters; ++i) {
+    const long long row = base + 8 * i;
+    if (row >= rows) break;
+    const int p = static_cast<int>(row % N);
+    if (i == 0 || p < 8) {
+      rope_row(lo_tab, hi_tab, p, u, e);
+    } else {
+#pragma unroll
+      for (int w = 0; w < 8; ++w)
+        e[w] = make_float2(e[w].x * step[w].x - e[w].y * step[w].y, e[w].x * step[w].y + e[w].y * step[w].x);
+    }
+    const uint32_t xa[4] = {ka[i].x, ka[i].y, ka[i].z, ka[i].w}, xb[4] = {kb[i].x, kb[i].y, kb[i].z, kb[i].w};
+    uint32_t ya[4], yb[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      // (k_m, k_{m+32}) -> (k_m cos - k_{m+32} sin, k_m sin + k_{m+32} cos), m = 8u + 2c (+1)
+      const float k1x = bf_lo(xa[c]), k1y = bf_hi(xa[c]), k2x = bf_lo(xb[c]), k2y = bf_hi(xb[c]);
+      const float2 e0 = e[2 * c], e1 = e[2 * c + 1];
+      ya[c] = pack_h2(k1x * e0.x - k2x * e0.y, k1y * e1.x - k2y * e1.y);
+      yb[c] = pack_h2(k1x * e0.y + k2x * e0.x, k1y * e1.y + k2y * e1.x);
+    }
+    const uint32_t wa[4] = {va[i].x, va[i].y, va[i].z, va[i].w}, wb[4] = {vb[i].x, vb[i].y, vb[i].z, vb[i].w};
+    uint32_t za[4], zb[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      za[c] = pack_h2(bf_lo(wa[c]), bf_hi(wa[c]));
+      zb[c] = pack_h2(bf_lo(wb[c]), bf_hi(wb[c]));
+    }
+    // A rotated key or a value beyond the float16 range (|x| > 65504) cannot be represented
+    // in the prepared rows: record it (the outputs of this call are then unspecified).
+#pragma unroll
+    for (int c = 0; c < 4; ++c) bad |= h2_nonfinite(ya[c]) | h2_nonfinite(yb[c]) | h2_nonfinite(za[c]) | h2_nonfinite(zb[c]);
+    const int sw = swz(p);
+    uint4* ko = reinterpret_cast<uint4*>(kp + row * kD);
+    uint4* vo = reinterpret_cast<uint4*>(vp + row * kD);
+    ko[u ^ sw] = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+    ko[(u + 4) ^ sw] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+    vo[u ^ sw] = make_uint4(za[0], za[1], za[2], za[3]);
+    vo[(u + 4) ^ sw] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
+  }
   if (bad) atomicExch(status, kStatusRange);
-  const int sw = swz(p);
-  uint4* ko = reinterpret_cast<uint4*>(kp + row * kD);
-  uint4* vo = reinterpret_cast<uint4*>(vp + row * kD);
-  ko[u ^ sw] = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-  ko[(u + 4) ^ sw] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
-  vo[u ^ sw] = make_uint4(za[0], za[1], za[2], za[3]);
-  vo[(u + 4) ^ sw] = make_uint4(zb[0], zb[1], zb[2], zb[3]);
 }
 
 // ------------------------------------------------------------------ attention kernel
@@ -647,9 +688,9 @@ cudaError_t launch_prep_kv(int B, int H, int N, const void* k, const void* v, co
   const long long rows = static_cast<long long>(B) * H * N;
   __half* kp = static_cast<__half*>(workspace);
   __half* vp = kp + rows * kD;
-  const long long blocks = (rows * 4 + 255) / 256;  // four threads a row
+  const long long blocks = (rows + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  prep_kv_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+  prep_kv_kernel<<<static_cast<unsigned>(blocks), kPrepThreads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), kp, vp, lo_tab, hi_tab, N,
       rows, status);
   return cudaGetLastError();
