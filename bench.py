@@ -96,10 +96,15 @@ def read_peaks():
 
 
 def source_hash(files):
+    """Hash of the code of the named kernel sources: `//` comments, surrounding blanks and
+    empty lines are left out, so that a profile summary stays valid across comment edits."""
     h = hashlib.sha256()
     for fn in files:
-        with open(os.path.join(ROOT, "fibonacci_offset_sparse_gb300", "csrc", fn), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "fibonacci_offset_sparse_gb300", "csrc", fn)) as f:
+            for line in f:
+                code = line.split("//", 1)[0].strip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

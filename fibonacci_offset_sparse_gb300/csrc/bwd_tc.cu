@@ -9,21 +9,23 @@
 //   dq_i = R(i)^T sum dS wt k'_j / 8      dk_j = R(j)^T sum dS wt q'_i / 8      dv_j = sum P wt dO_i
 // over the (query, key row) pairs with blend weight wt (1 for window and mask keys).
 //
-// Three launches:
+// The (b, h) rows run as two halves (one when B*H = 1), the second on a side stream, each
+// as three launches:
 //   * bwd_prep_kernel: Q's = RoPE(q) log2(e)/8, K' = RoPE(k), V' = v and dO' = dO, all f16
 //     with the chunk swizzle of fwd_tc.cu, and Delta (float32), each row read once.
 //   * bwd_q_kernel (query-owned, 64 queries a CTA): the forward's structure, with dP =
 //     dO'.V'^T beside S = Q's.K'^T and dq' += dS K' in place of O += P V'.  Rungs are
 //     diagonals of 16x16 blocks, as in the forward (interp: one 24-row band per operand
 //     gives the row and its partner).  It also writes P and dS of every attended (query,
-//     key slot) -- W + R float pairs a query, the sparse pattern makes that small -- and
-//     each CTA's dalpha partial.
+//     key slot) -- W + R float pairs a query, the sparse pattern makes that small; stored
+//     slot-major, so that a slot's run of consecutive queries is contiguous -- and each
+//     CTA's dalpha partial.
 //   * bwd_kv_kernel (key-owned, 64 keys a CTA, no atomics): a gather, no score is
 //     recomputed.  The queries that read the CTA's keys stream through a ring (the 80-row
 //     block [j0, j0+80) of Q's and dO' for the window band, then per rung the query slab
-//     [j0+lo, j0+lo+65)); with their stored P and dS (loaded one rung ahead), dk' += dS^T
-//     Q's and dv += P^T dO'.
-//     Its CTA 0 also sums the dQ grid's dalpha partials in a fixed order.
+//     [j0+lo, j0+lo+65) with its run of stored P and dS), dk' += dS^T Q's and dv += P^T dO'.
+//     In the half that sums it, its CTA 0 also adds the dalpha partials of both halves'
+//     dQ grids in a fixed order.
 // Precision as the forward: f16 operands (Q's, K', V', dO', P, dS), f32 accumulation.
 #include <algorithm>
 #include <type_traits>
