@@ -675,6 +675,13 @@ def main():
                          "attend_achieved_gbs": ach, "attend_frac": ach / peak,
                          "layer_frac": compulsory_bytes(ws) / ls / 1e9 / peak, "traffic": ncu_traffic(name)}
         line["secondary"] = sec
+        # the interpolated path's cost over the mask path on the same shapes (the pages quote
+        # ~5x for their own implementation, hardware unstated)
+        line["interp_over_mask"] = {
+            "n1024_layer": sec["learned-interp-n1024"]["us_per_layer"] / (r["ms_per_step"] * 1e3 / WORKLOADS[DEFAULT]["L"]),
+            "n131072_layer": sec["long-interp-n131072"]["us_per_layer"] / sec["long-mask-n131072"]["us_per_layer"],
+            "note": "N=1024: learned-interp-n1024 (W=10) over linear-stack-n1024 (W=12); N=131072: same shape and W",
+            "pages_quote": "~5x (hardware unstated)"}
         wb = WORKLOADS[BACKWARD]
         rb = time_backward(wb, args.steps, args.warmup, device)
         bb = compulsory_bytes_bwd(wb)
