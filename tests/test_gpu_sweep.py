@@ -1,4 +1,4 @@
-"""Seeded random sweep of the forward and the backward against the float64 oracle.
+"""Seeded random sweep of the forward, the backward and decode against the float64 oracle.
 
 The hand-picked parity cases pin the configurations the pages measure and the known edge
 cases; this sweep draws 96 more cases from one fixed seed, over lengths 1..2500 (log-uniform,
@@ -8,7 +8,8 @@ power-of-two bases, both modes, one to six (b, h) rows (B*H = 1 runs the backwar
 alpha from the plan or from the device.  Tolerances are those of the parity tests, with an
 absolute floor for gradients whose reference is (near) zero, e.g. N = 1 where dS vanishes:
   * O: max-abs <= 1e-2 beyond the bf16 output's own rounding (2^-8 |O|), 1e-5 float32;
-  * LSE: 5e-3 (bf16), 1e-5 (float32);
+  * LSE: 5e-3 (bf16), 1e-5 (float32); decode (one row, pos drawn per case): O as above,
+    LSE 1e-3 (bf16: the decode kernel computes in float32 from the bf16 values), 1e-5;
   * dQ, dK, dV: ||g - r|| <= 2e-2 ||r|| + 1e-3 sqrt(n) (bf16), 1e-5 ||r|| + 1e-7 sqrt(n);
   * dalpha: within 2e-2 (1e-4 float32) of the larger of |dalpha| and the root-sum-square
     of its per-(b, h) contributions, plus 1e-4; exactly 0 in mask mode.
@@ -73,6 +74,8 @@ def test_random_case_forward_and_backward_match_the_oracle(case):
     qc, kc, vc, gc = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
     o, lse = fa.fib_attn_fwd(plan, 0, qc, kc, vc, alpha_dev=adev)
     dq, dk, dv, da = fa.fib_attn_bwd(plan, 0, qc, kc, vc, o, lse, gc, alpha_dev=adev)
+    pos = (7919 * i) % N  # one decode step against the whole cache: row pos of the forward
+    od, lsed = fa.fib_attn_decode(plan, 0, pos, qc[:, :, pos].contiguous(), kc, vc, alpha_dev=adev)
     torch.cuda.synchronize()
     assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
     plan.close()
@@ -84,6 +87,9 @@ def test_random_case_forward_and_backward_match_the_oracle(case):
     o_err = np.abs(o.double().cpu().numpy() - O_ref) - (2.0 ** -8 * np.abs(O_ref) if bf else 0.0)
     assert o_err.max() <= (1e-2 if bf else 1e-5)
     assert np.abs(lse.double().cpu().numpy() - lse_ref).max() <= (5e-3 if bf else 1e-5)
+    d_err = np.abs(od.double().cpu().numpy() - O_ref[:, :, pos]) - (2.0 ** -8 * np.abs(O_ref[:, :, pos]) if bf else 0.0)
+    assert d_err.max() <= (1e-2 if bf else 1e-5)
+    assert np.abs(lsed.double().cpu().numpy() - lse_ref[:, :, pos]).max() <= (1e-3 if bf else 1e-5)
 
     rq, rk, rv = np.zeros_like(qf), np.zeros_like(kf), np.zeros_like(vf)
     per = []
