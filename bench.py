@@ -415,9 +415,12 @@ def time_device(w, steps, warmup, device, rank, world):
     return res
 
 
-def time_backward(w, steps, warmup, device):
+def time_backward(w, steps, warmup, device, prepared=True):
     """Backward of the L-layer stack (dQ, dK, dV and dalpha of every layer), replayed from a
-    CUDA graph: milliseconds per step and per launch of the backward."""
+    CUDA graph: milliseconds per step and per launch of the backward.  prepared: each layer's
+    backward takes the K'/V' rows its forward prepared (fib_attn_bwd_prepared, as a training
+    step that keeps the forward's workspace does); else it prepares them from k and v
+    (fib_attn_bwd)."""
     import torch
     from fibonacci_offset_sparse_gb300 import fib_attn as fa
     from fibonacci_offset_sparse_gb300 import inputs
@@ -436,8 +439,12 @@ def time_backward(w, steps, warmup, device):
 
     def bwd_stack():
         for l, (q, k, v) in enumerate(dev):
-            fa.fib_attn_bwd(plan, l, q, k, v, outs[l], lses[l], dOs[l], *grads[l], dalpha=dal[l],
-                            alpha_dev=adev, workspace=bws[l])
+            if prepared:  # wss[l]: layer l's forward workspace, filled by run_stack above
+                fa.fib_attn_bwd_prepared(plan, l, q, wss[l], outs[l], lses[l], dOs[l], *grads[l], dalpha=dal[l],
+                                         alpha_dev=adev, workspace=bws[l])
+            else:
+                fa.fib_attn_bwd(plan, l, q, k, v, outs[l], lses[l], dOs[l], *grads[l], dalpha=dal[l],
+                                alpha_dev=adev, workspace=bws[l])
 
     with torch.cuda.stream(stream):
         bwd_stack()
@@ -684,12 +691,19 @@ def main():
             "pages_quote": "~5x (hardware unstated)"}
         wb = WORKLOADS[BACKWARD]
         rb = time_backward(wb, args.steps, args.warmup, device)
+        rb_alone = time_backward(wb, args.steps, args.warmup, device, prepared=False)
         bb = compulsory_bytes_bwd(wb)
         dec = {m: time_decode(m, 1, 8, 4096, 16, args.steps, args.warmup, device) for m in ("mask", "interp")}
         line["decode"] = {"shape": "B=1, H=8, 16 layers, cache N=4096, new token at 4095, W=12, alpha=1.5",
                           "mask_us_per_token": dec["mask"], "interp_us_per_token": dec["interp"],
                           "interp_over_mask": dec["interp"] / dec["mask"]}
-        line["backward"] = {"workload": BACKWARD, "path": "interp backward (dQ, dK, dV, dalpha)",
+        line["backward"] = {"workload": BACKWARD,
+                            "path": "interp backward (dQ, dK, dV, dalpha) from the forward's prepared K'/V' rows "
+                                    "(fib_attn_bwd_prepared)",
+                            "standalone": {"path": "fib_attn_bwd: K'/V' prepared from k and v in the backward",
+                                           "ms_per_step": rb_alone["ms_per_step"],
+                                           "us_per_layer": rb_alone["us_per_layer"],
+                                           "frac": compulsory_bytes_bwd(wb) / (rb_alone["us_per_layer"] * 1e-6) / 1e9 / peak},
                             "value": wb["B"] * wb["N"] * world / (rb["ms_per_step"] / 1e3), "unit": UNIT,
                             "ms_per_step": rb["ms_per_step"], "us_per_layer": rb["us_per_layer"],
                             "compulsory_bytes_per_layer": bb,

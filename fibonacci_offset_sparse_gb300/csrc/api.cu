@@ -34,9 +34,9 @@ size_t bwd_workspace_bytes(int B, int H, int N);
 bool bwd_tc_supported(const LayerTable& t);
 size_t bwd_tc_workspace_bytes(int B, int H, int N, int W);
 cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k, const void* v,
-                          const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                          float* dalpha, void* ws, const float2* lo_tab, const float2* hi_tab, int* status,
-                          unsigned long long wait_ns, cudaStream_t stream, const BwdStreams& side);
+                          const void* kv_prepared, const void* o, const float* lse, const void* dO, void* dq,
+                          void* dk, void* dv, float* dalpha, void* ws, const float2* lo_tab, const float2* hi_tab,
+                          int* status, unsigned long long wait_ns, cudaStream_t stream, const BwdStreams& side);
 cudaError_t launch_bwd(const LayerTable& t, int B, int H, int N, int dtype, const void* q,
                        const void* k, const void* v, const void* o, const float* lse,
                        const void* dO, void* dq, void* dk, void* dv, float* dalpha, void* ws,
@@ -496,11 +496,49 @@ int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, c
   // otherwise the CUDA-core kernels (bwd.cu), which also serve float32
   if (dtype == FIB_DTYPE_BF16 && bwd_tc_supported(t)) {
     std::lock_guard<std::mutex> lock(p->side_mu);
-    return cuda_status(launch_bwd_tc(t, B, H, N, q, k, v, o, lse, dO, dq, dk, dv, dalpha, workspace, p->d_lo,
-                                     p->d_hi, p->d_status, p->wait_ns, static_cast<cudaStream_t>(stream), p->side));
+    return cuda_status(launch_bwd_tc(t, B, H, N, q, k, v, nullptr, o, lse, dO, dq, dk, dv, dalpha, workspace,
+                                     p->d_lo, p->d_hi, p->d_status, p->wait_ns, static_cast<cudaStream_t>(stream),
+                                     p->side));
   }
   return cuda_status(launch_bwd(t, B, H, N, dtype, q, k, v, o, lse, dO, dq, dk, dv, dalpha,
                                 workspace, p->d_lo, p->d_hi, static_cast<cudaStream_t>(stream)));
+}
+
+// Backward from the forward's prepared K' and V' rows (bf16 tensor-core path only): the same
+// checks and kernels as fib_attn_bwd, minus the preparation of K' and V'.
+int fib_attn_bwd_prepared(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype, const void* q,
+                          const void* kv_prepared, size_t kv_bytes, const void* o, const float* lse,
+                          const void* dO, void* dq, void* dk, void* dv, float* dalpha, const float* alpha_dev,
+                          void* workspace, size_t ws_bytes, void* stream) {
+  int st = check_shape(p, layer, B, H, N, dtype);
+  if (st != FIB_OK) return st;
+  if (check_tensor(q) || check_tensor(o) || check_tensor(dO) || check_tensor(dq) || check_tensor(dk) ||
+      check_tensor(dv))
+    return FIB_ERR_INVALID_ARG;
+  if (lse == nullptr || !aligned(lse, 4) || dalpha == nullptr || !aligned(dalpha, 4)) return FIB_ERR_INVALID_ARG;
+  if (alpha_dev != nullptr && !aligned(alpha_dev, 4)) return FIB_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < fib_attn_bwd_workspace_size(p, B, H, N))
+    return FIB_ERR_INVALID_ARG;
+  const size_t kv_need = fib_attn_fwd_workspace_size(p, B, H, N, dtype);
+  if (kv_need == 0) return FIB_ERR_UNSUPPORTED;  // float32, or a window wider than 16
+  if (kv_prepared == nullptr || !aligned(kv_prepared, 256) || kv_bytes < kv_need) return FIB_ERR_INVALID_ARG;
+  const void* ins[] = {q, o, dO, kv_prepared};
+  const void* outs[] = {dq, dk, dv};
+  for (const void* a : outs)
+    for (const void* b : ins)
+      if (a == b) return FIB_ERR_INVALID_ARG;
+  if (dq == dk || dq == dv || dk == dv) return FIB_ERR_INVALID_ARG;
+  if (kv_prepared == workspace) return FIB_ERR_INVALID_ARG;
+  st = check_device(p);
+  if (st != FIB_OK) return st;
+  LayerTable t;
+  st = make_table(p, layer, N, p->mode == FIB_MODE_INTERP ? alpha_dev : nullptr, &t);
+  if (st != FIB_OK) return st;
+  if (!bwd_tc_supported(t)) return FIB_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(p->side_mu);
+  return cuda_status(launch_bwd_tc(t, B, H, N, q, nullptr, nullptr, kv_prepared, o, lse, dO, dq, dk, dv, dalpha,
+                                   workspace, p->d_lo, p->d_hi, p->d_status, p->wait_ns,
+                                   static_cast<cudaStream_t>(stream), p->side));
 }
 
 // Backward for callers that cannot allocate device memory: the same checks and kernels as

@@ -118,7 +118,9 @@ __device__ __forceinline__ void store_plain(__nv_bfloat16* row, const float (&ac
 
 // ------------------------------------------------------------------ preparation
 // One thread per (row, quarter u), frequencies m = 8u .. 8u+7 (chunks u and u+4 of a row):
-// the four f16 arrays, and Delta by a quad reduction.
+// the four f16 arrays, and Delta by a quad reduction.  Without KV (K' and V' prepared by the
+// layer's forward and handed over), only Q's, dO' and Delta.
+template <bool KV>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ q,
                                                        const __nv_bfloat16* __restrict__ k,
                                                        const __nv_bfloat16* __restrict__ v,
@@ -140,9 +142,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   const int p = static_cast<int>(row % N);
   const size_t off = static_cast<size_t>(row) * kD;
   auto ld = [&](const __nv_bfloat16* base, int c) { return __ldcs(reinterpret_cast<const uint4*>(base + off) + c); };
-  const uint4 qa = ld(q, u), qb = ld(q, u + 4), ka = ld(k, u), kb = ld(k, u + 4);
-  const uint4 va = ld(v, u), vb = ld(v, u + 4), ga = ld(dO, u), gb = ld(dO, u + 4);
+  const uint4 qa = ld(q, u), qb = ld(q, u + 4), ga = ld(dO, u), gb = ld(dO, u + 4);
   const uint4 oa = ld(o, u), ob = ld(o, u + 4);
+  uint4 ka, kb, va, vb;
+  if (KV) ka = ld(k, u), kb = ld(k, u + 4), va = ld(v, u), vb = ld(v, u + 4);
   float2 e[8];
   rope_row(lo_tab, hi_tab, p, u, e);
   auto rotate = [&](const uint4& xa4, const uint4& xb4, float sc, uint4& ya4, uint4& yb4) {
@@ -176,12 +179,16 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   rotate(qa, qb, qscale, ya, yb);
   chk(ya); chk(yb);
   put(qs, ya, yb);
-  rotate(ka, kb, 1.f, ya, yb);
-  chk(ya); chk(yb);
-  put(kp, ya, yb);
-  const uint4 vha = to_h(va), vhb = to_h(vb), gha = to_h(ga), ghb = to_h(gb);
-  chk(vha); chk(vhb); chk(gha); chk(ghb);
-  put(vp, vha, vhb);
+  if (KV) {
+    rotate(ka, kb, 1.f, ya, yb);
+    chk(ya); chk(yb);
+    put(kp, ya, yb);
+    const uint4 vha = to_h(va), vhb = to_h(vb);
+    chk(vha); chk(vhb);
+    put(vp, vha, vhb);
+  }
+  const uint4 gha = to_h(ga), ghb = to_h(gb);
+  chk(gha); chk(ghb);
   put(dos, gha, ghb);
   if (bad) atomicExch(status, kStatusRange);
   // Delta = dO . O over the row (float32 from the bf16 values)
@@ -797,9 +804,11 @@ namespace {
 // dalpha when dalpha is not null.  record_after_q, when given, is recorded between the dQ and
 // the dK/dV launch (it marks the end of the dQ grid for the other half); wait_before_kv, when
 // given, is an event the dK/dV launch waits for first (the other half's dQ grid, whose
-// partials it sums too).
+// partials it sums too).  kv_k, kv_v: the whole call's K' and V' rows prepared by the layer's
+// forward (the half's rows are read at its offset), or null to prepare them here.
 cudaError_t launch_half(const LayerTable& t, long long off, long long n, int N, const void* q, const void* k,
-                        const void* v, const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                        const void* v, const __half* kv_k, const __half* kv_v, const void* o, const float* lse,
+                        const void* dO, void* dq, void* dk, void* dv,
                         float* partials, long long n_before, long long n_sum, float* dalpha, unsigned char* w,
                         const float2* lo_tab, const float2* hi_tab, int* status, unsigned long long wait_ns,
                         cudaEvent_t record_after_q, cudaEvent_t wait_before_kv, cudaStream_t stream) {
@@ -815,8 +824,8 @@ cudaError_t launch_half(const LayerTable& t, long long off, long long n, int N, 
   a.bh = static_cast<int>(n);
   a.qs = reinterpret_cast<const __half*>(w);
   a.dos = reinterpret_cast<const __half*>(w + arr);
-  a.kp = reinterpret_cast<const __half*>(w + 2 * arr);
-  a.vp = reinterpret_cast<const __half*>(w + 3 * arr);
+  a.kp = kv_k != nullptr ? kv_k + eo : reinterpret_cast<const __half*>(w + 2 * arr);
+  a.vp = kv_v != nullptr ? kv_v + eo : reinterpret_cast<const __half*>(w + 3 * arr);
   float* delta = reinterpret_cast<float*>(w + 4 * arr);
   a.delta = delta;
   a.pds = reinterpret_cast<float2*>(w + 4 * arr + up256(static_cast<size_t>(rows) * sizeof(float)));
@@ -832,9 +841,14 @@ cudaError_t launch_half(const LayerTable& t, long long off, long long n, int N, 
   const long long blocks = static_cast<long long>(a.tiles) * n;
   const long long prep_blocks = (rows * 4 + 255) / 256;
   if (blocks > 0x7fffffffLL || prep_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  bwd_prep_kernel<<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
-      bf(q), bf(k), bf(v), bf(o), bf(dO), const_cast<__half*>(a.qs), const_cast<__half*>(a.kp),
-      const_cast<__half*>(a.vp), const_cast<__half*>(a.dos), delta, lo_tab, hi_tab, N, rows, kLog2e / 8.0f, status);
+  if (kv_k == nullptr)
+    bwd_prep_kernel<true><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
+        bf(q), bf(k), bf(v), bf(o), bf(dO), const_cast<__half*>(a.qs), const_cast<__half*>(a.kp),
+        const_cast<__half*>(a.vp), const_cast<__half*>(a.dos), delta, lo_tab, hi_tab, N, rows, kLog2e / 8.0f, status);
+  else
+    bwd_prep_kernel<false><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
+        bf(q), nullptr, nullptr, bf(o), bf(dO), const_cast<__half*>(a.qs), nullptr, nullptr,
+        const_cast<__half*>(a.dos), delta, lo_tab, hi_tab, N, rows, kLog2e / 8.0f, status);
   cudaError_t e;
   // query-owned: dq and the dalpha partials
   a.partials = partials + n_before;
@@ -900,9 +914,9 @@ cudaError_t launch_half(const LayerTable& t, long long off, long long n, int N, 
 }  // namespace
 
 cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* q, const void* k, const void* v,
-                          const void* o, const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                          float* dalpha, void* ws, const float2* lo_tab, const float2* hi_tab, int* status,
-                          unsigned long long wait_ns, cudaStream_t stream, const BwdStreams& side) {
+                          const void* kv_prepared, const void* o, const float* lse, const void* dO, void* dq,
+                          void* dk, void* dv, float* dalpha, void* ws, const float2* lo_tab, const float2* hi_tab,
+                          int* status, unsigned long long wait_ns, cudaStream_t stream, const BwdStreams& side) {
   // The (b, h) rows run as two halves, the second on the side stream (forked from and joined
   // back to `stream` with events): each half's grids then fill the SMs that the other half's
   // last, partly filled wave of CTAs leaves idle.  The first half's dK/dV grid leaves dalpha
@@ -915,16 +929,19 @@ cudaError_t launch_bwd_tc(const LayerTable& t, int B, int H, int N, const void* 
   float* partials = reinterpret_cast<float*>(w);
   unsigned char* w0 = w + up256(static_cast<size_t>(tiles * bh) * sizeof(float));
   unsigned char* w1 = w0 + half_bytes(bh0, N, t.W);
+  // the layer's forward workspace, when handed over: K' rows of the whole call, then its V'
+  const __half* kv_k = static_cast<const __half*>(kv_prepared);
+  const __half* kv_v = kv_k != nullptr ? kv_k + static_cast<size_t>(bh) * N * kD : nullptr;
   if (bh == bh0)
-    return launch_half(t, 0, bh, N, q, k, v, o, lse, dO, dq, dk, dv, partials, 0, tiles * bh, dalpha, w0, lo_tab,
+    return launch_half(t, 0, bh, N, q, k, v, kv_k, kv_v, o, lse, dO, dq, dk, dv, partials, 0, tiles * bh, dalpha, w0, lo_tab,
                        hi_tab, status, wait_ns, nullptr, nullptr, stream);
   cudaError_t e = cudaEventRecord(side.fork, stream);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.fork, 0);
   if (e == cudaSuccess)
-    e = launch_half(t, 0, bh0, N, q, k, v, o, lse, dO, dq, dk, dv, partials, 0, 0, nullptr, w0, lo_tab, hi_tab,
+    e = launch_half(t, 0, bh0, N, q, k, v, kv_k, kv_v, o, lse, dO, dq, dk, dv, partials, 0, 0, nullptr, w0, lo_tab, hi_tab,
                     status, wait_ns, side.first_q_done, nullptr, stream);
   if (e == cudaSuccess)
-    e = launch_half(t, bh0, bh - bh0, N, q, k, v, o, lse, dO, dq, dk, dv, partials, tiles * bh0, tiles * bh, dalpha,
+    e = launch_half(t, bh0, bh - bh0, N, q, k, v, kv_k, kv_v, o, lse, dO, dq, dk, dv, partials, tiles * bh0, tiles * bh, dalpha,
                     w1, lo_tab, hi_tab, status, wait_ns, nullptr, side.first_q_done, side.stream);
   if (e == cudaSuccess) e = cudaEventRecord(side.join, side.stream);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, side.join, 0);

@@ -31,7 +31,7 @@ EXPORTS = [
     "fib_attn_fwd_prepare_kv", "fib_attn_fwd_attend", "fib_attn_bwd_workspace_size", "fib_attn_bwd",
     "fib_attn_debug_indices", "fib_attn_last_device_status", "fib_attn_plan_set_debug",
     "fib_attn_bwd_noalloc", "fib_attn_decode", "fib_attn_dense_fwd_workspace_size", "fib_attn_dense_fwd",
-    "fib_attn_debug_fill_shared",
+    "fib_attn_debug_fill_shared", "fib_attn_bwd_prepared",
 ]
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -68,6 +68,8 @@ _SIGS = {
     "fib_attn_dense_fwd": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "fib_attn_bwd_noalloc": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                   _vp, _vp, _vp, _vp]),
+    "fib_attn_bwd_prepared": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp,
+                                   _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
 }
 
 _lib = None
@@ -321,6 +323,29 @@ def fib_attn_bwd(plan: Plan, layer: int, q, k, v, o, lse, dO, dq=None, dk=None, 
         plan.handle, layer, B, H, N, _DT[q.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
         _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha), _ptr(alpha_dev), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dq, dk, dv, dalpha
+
+
+def fib_attn_bwd_prepared(plan: Plan, layer: int, q, kv_prepared, o, lse, dO, dq=None, dk=None, dv=None,
+                          dalpha=None, alpha_dev=None, workspace=None, stream=None):
+    """Backward from the forward's prepared K'/V' rows (the uint8 workspace that
+    fib_attn_fwd or fib_attn_fwd_prepare_kv filled for this layer's k and v): returns
+    (dq, dk, dv, dalpha[1]), those of fib_attn_bwd up to the float16 rounding of K'."""
+    B, H, N = _shape(q)
+    _same(q, o, dO, dq, dk, dv)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    if dalpha is None:
+        dalpha = torch.empty(1, dtype=torch.float32, device=q.device)
+    need = fib_attn_bwd_workspace_size(plan, B, H, N)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check("fib_attn_bwd_prepared", lib().fib_attn_bwd_prepared(
+        plan.handle, layer, B, H, N, _DT[q.dtype], _ptr(q), _ptr(kv_prepared),
+        kv_prepared.numel() * kv_prepared.element_size(), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+        _ptr(dv), _ptr(dalpha), _ptr(alpha_dev), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
     return dq, dk, dv, dalpha
 
 

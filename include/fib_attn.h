@@ -222,8 +222,9 @@ int fib_attn_decode(fib_attn_plan_t p, int layer, int B, int H, int N, int pos, 
  * workspace: device scratch of at least fib_attn_bwd_workspace_size(p, B, H, N) bytes,
  * 256-byte aligned, caller-owned; its contents on entry are ignored.  The size is the same
  * for both dtypes: for a plan with W <= 16 it is what the bf16 path needs (Q, K, V, dO
- * prepared once as float16 rows, B*H*N*512 bytes, plus Delta and the dalpha partials);
- * the float32 path uses only the first B*H*N*4 bytes and the partials.
+ * prepared once as float16 rows, B*H*N*512 bytes; Delta; the (P, dS) float pair of every
+ * attended (query, key slot); the dalpha partials); the float32 path uses only its first
+ * B*H*N*4 bytes and the partials.
  * Streams: on the bf16 tensor-core path with B*H >= 2, the second half of the (b, h) rows
  * runs on a stream the plan owns, forked from `stream` and joined back to it with events
  * before the call returns (so that work enqueued on `stream` afterwards, and a stream
@@ -237,6 +238,27 @@ int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
                  const float* lse, const void* dO, void* dq, void* dk, void* dv,
                  float* dalpha, const float* alpha_dev, void* workspace, size_t ws_bytes,
                  void* stream);
+
+/* Backward from the forward's prepared rows.  K' (RoPE at each row's own position) and V'
+ * as float16 rows are what the bf16 forward prepares in its workspace and what the bf16
+ * backward needs of k and v ("Implementation": RoPE is applied before the rows are
+ * gathered, in both passes); a training step that keeps that workspace from the layer's
+ * forward (fib_attn_fwd or fib_attn_fwd_prepare_kv of the same plan, B, H, N and the same k
+ * and v, not checked) hands it over here instead of k and v, and the backward prepares
+ * only Q', dO' and Delta.  Results equal those of fib_attn_bwd on the same inputs up to the
+ * float16 rounding of K' (the forward builds the RoPE factors of three rows in four by a
+ * recurrence, the backward's own preparation reads them from the tables, so a K' element
+ * can differ in its last bit); both are deterministic.  kv_prepared: that workspace,
+ * kv_bytes >= fib_attn_fwd_workspace_size(p, B, H, N,
+ * dtype), 256-byte aligned, read only.  Everything else as fib_attn_bwd, plus
+ * FIB_ERR_UNSUPPORTED where the forward has no prepared rows (float32, or W > 16: call
+ * fib_attn_bwd there) and FIB_ERR_INVALID_ARG for a short or misaligned kv_prepared or one
+ * that is the backward workspace or an output.                                          */
+int fib_attn_bwd_prepared(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
+                          const void* q, const void* kv_prepared, size_t kv_bytes, const void* o,
+                          const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                          float* dalpha, const float* alpha_dev, void* workspace, size_t ws_bytes,
+                          void* stream);
 
 /* Backward without allocation.  The paper has no counterpart: this is an interface for
  * callers that cannot allocate device memory on the call path -- for example a plugin inside

@@ -30,9 +30,17 @@ def test_autograd_is_the_library_forward_and_backward(dtype):
     g = inputs.upstream_grad(B, H, N, 64, 300, 1, dtype).cuda()
     o = fib_attention(plan, 1, q, k, v, alpha)
     o.backward(g)
-    o2, lse2 = fa.fib_attn_fwd(plan, 1, q.detach(), k.detach(), v.detach(), alpha_dev=alpha.detach())
-    dq, dk, dv, da = fa.fib_attn_bwd(plan, 1, q.detach(), k.detach(), v.detach(), o2, lse2, g,
-                                     alpha_dev=alpha.detach())
+    # the Function keeps the forward's prepared K'/V' where there are any (bf16) and starts
+    # the backward from them
+    need = fa.fib_attn_fwd_workspace_size(plan, B, H, N, q.dtype)
+    kv = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    o2, lse2 = fa.fib_attn_fwd(plan, 1, q.detach(), k.detach(), v.detach(), alpha_dev=alpha.detach(),
+                               workspace=kv if need else None)
+    if need:
+        dq, dk, dv, da = fa.fib_attn_bwd_prepared(plan, 1, q.detach(), kv, o2, lse2, g, alpha_dev=alpha.detach())
+    else:
+        dq, dk, dv, da = fa.fib_attn_bwd(plan, 1, q.detach(), k.detach(), v.detach(), o2, lse2, g,
+                                         alpha_dev=alpha.detach())
     assert torch.equal(o, o2)
     assert torch.equal(q.grad, dq) and torch.equal(k.grad, dk) and torch.equal(v.grad, dv)
     assert float(alpha.grad[1]) == float(da[0]) and float(alpha.grad[0]) == 0.0 == float(alpha.grad[2])
