@@ -415,12 +415,13 @@ def time_device(w, steps, warmup, device, rank, world):
     return res
 
 
-def time_backward(w, steps, warmup, device, prepared=True):
+def time_backward(w, steps, warmup, device, prepared=True, with_forward=False):
     """Backward of the L-layer stack (dQ, dK, dV and dalpha of every layer), replayed from a
     CUDA graph: milliseconds per step and per launch of the backward.  prepared: each layer's
     backward takes the K'/V' rows its forward prepared (fib_attn_bwd_prepared, as a training
     step that keeps the forward's workspace does); else it prepares them from k and v
-    (fib_attn_bwd)."""
+    (fib_attn_bwd).  with_forward: the graph holds the forward of the stack, then its
+    backward (a training step's attention: the layers' forwards keep their workspaces)."""
     import torch
     from fibonacci_offset_sparse_gb300 import fib_attn as fa
     from fibonacci_offset_sparse_gb300 import inputs
@@ -438,6 +439,8 @@ def time_backward(w, steps, warmup, device, prepared=True):
     bws = [torch.empty(need, dtype=torch.uint8, device=device)] * len(dev)
 
     def bwd_stack():
+        if with_forward:
+            run_stack(fa, plan, dev, outs, lses, adev, wss)
         for l, (q, k, v) in enumerate(dev):
             if prepared:  # wss[l]: layer l's forward workspace, filled by run_stack above
                 fa.fib_attn_bwd_prepared(plan, l, q, wss[l], outs[l], lses[l], dOs[l], *grads[l], dalpha=dal[l],
@@ -692,6 +695,7 @@ def main():
         wb = WORKLOADS[BACKWARD]
         rb = time_backward(wb, args.steps, args.warmup, device)
         rb_alone = time_backward(wb, args.steps, args.warmup, device, prepared=False)
+        rt = time_backward(wb, args.steps, args.warmup, device, with_forward=True)
         bb = compulsory_bytes_bwd(wb)
         dec = {m: time_decode(m, 1, 8, 4096, 16, args.steps, args.warmup, device) for m in ("mask", "interp")}
         line["decode"] = {"shape": "B=1, H=8, 16 layers, cache N=4096, new token at 4095, W=12, alpha=1.5",
@@ -710,6 +714,14 @@ def main():
                             "achieved_gbs": bb / (rb["us_per_layer"] * 1e-6) / 1e9,
                             "frac": bb / (rb["us_per_layer"] * 1e-6) / 1e9 / peak,
                             "traffic": ncu_traffic_bwd(BACKWARD)}
+        tb = compulsory_bytes(wb) + bb
+        line["train_step"] = {"workload": BACKWARD,
+                              "path": "forward of the stack, then its backward from the kept K'/V' (one graph)",
+                              "value": wb["B"] * wb["N"] * world / (rt["ms_per_step"] / 1e3), "unit": UNIT,
+                              "ms_per_step": rt["ms_per_step"], "us_per_layer": rt["us_per_layer"],
+                              "compulsory_bytes_per_layer": tb,
+                              "achieved_gbs": tb / (rt["us_per_layer"] * 1e-6) / 1e9,
+                              "frac": tb / (rt["us_per_layer"] * 1e-6) / 1e9 / peak}
     dense = {}
     for name in [args.workload] + (SECONDARY if args.workload == DEFAULT and not args.no_secondary else []):
         ws = WORKLOADS[name]
