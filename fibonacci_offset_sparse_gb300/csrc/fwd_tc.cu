@@ -270,8 +270,9 @@ __global__ void __launch_bounds__(kTcThreads, MODE == 0 ? FIB_TC_MIN_CTAS : FIB_
   const int nrt = 32 - __clz(static_cast<int>(attended));
   // Rungs whose slab lies inside the near block (ascending distances: a prefix) are served
   // from it, up to kMaxNear of them (per path, set by measurement: each near rung holds its
-  // scores in registers until the window's P.V); every other rung streams its own slab.
-  constexpr int kMaxNear = MODE == 0 ? 5 : 4;
+  // scores in registers until the window's P.V, which costs more on the interpolated path,
+  // where the rung step already holds more); every other rung streams its own slab.
+  constexpr int kMaxNear = MODE == 0 ? 4 : 1;
   const int n_near = min(kMaxNear, __popc(__ballot_sync(0xffffffffu, lane < nrt && rung_lo(lane) + kI <= kNear)));
   const int n_stages = 3 + nrt - n_near;  // Q, near K', near V', then one per streamed rung
 
