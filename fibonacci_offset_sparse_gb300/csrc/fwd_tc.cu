@@ -94,7 +94,7 @@ struct TcArgs {
 };
 
 // ------------------------------------------------------------------ K', V' preparation
-// A warp prepares 32 consecutive rows: lane (j8 = lane/4, u = lane%4) handles rows
+// A warp prepares 8 * kPrepIters consecutive rows: lane (j8 = lane/4, u = lane%4) handles rows
 // base + 8i + j8 (i < kPrepIters) and the frequencies m = 8u .. 8u+7, i.e. chunks u (dims
 // 8u..) and u+4 (their rotate-half partners 32+8u..) of the K row, and the same two chunks
 // of V.  Every load of the warp is issued first.  The RoPE factors e^{i p theta_m} of the
@@ -103,9 +103,9 @@ struct TcArgs {
 // each, relative error ~1e-7 a step, far below the float16 rounding of K'), unless a new
 // sequence began in between (position < 8), where the tables are read again.  This keeps
 // the table reads at a few bytes a row instead of 128.
-constexpr int kPrepIters = 4;
+constexpr int kPrepIters = 3;
 constexpr int kPrepThreads = 128;
-constexpr int kPrepRowsPerBlock = kPrepThreads / 4 * kPrepIters;  // 128
+constexpr int kPrepRowsPerBlock = kPrepThreads / 4 * kPrepIters;  // 96
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kv_kernel(const __nv_bfloat16* __restrict__ k,
                                                                const __nv_bfloat16* __restrict__ v,
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kv_kernel(const __nv_bfloat
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int u = lane & 3, j8 = lane >> 2;
-  const long long base = static_cast<long long>(blockIdx.x) * kPrepRowsPerBlock + (threadIdx.x >> 5) * 32 + j8;
+  const long long base = static_cast<long long>(blockIdx.x) * kPrepRowsPerBlock + (threadIdx.x >> 5) * (8 * kPrepIters) + j8;
   uint4 ka[kPrepIters], kb[kPrepIters], va[kPrepIters], vb[kPrepIters];
 #pragma unroll
   for (int i = 0; i < kPrepIters; ++i) {

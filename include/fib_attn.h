@@ -246,7 +246,7 @@ int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
  * forward (fib_attn_fwd or fib_attn_fwd_prepare_kv of the same plan, B, H, N and the same k
  * and v, not checked) hands it over here instead of k and v, and the backward prepares
  * only Q', dO' and Delta.  Results equal those of fib_attn_bwd on the same inputs up to the
- * float16 rounding of K' (the forward builds the RoPE factors of three rows in four by a
+ * float16 rounding of K' (the forward builds the RoPE factors of two rows in three by a
  * recurrence, the backward's own preparation reads them from the tables, so a K' element
  * can differ in its last bit); both are deterministic.  kv_prepared: that workspace,
  * kv_bytes >= fib_attn_fwd_workspace_size(p, B, H, N,

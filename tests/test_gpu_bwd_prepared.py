@@ -2,7 +2,7 @@
 
 The forward's workspace holds K' = RoPE(k) at each row's own position and V' as float16
 rows, what the bf16 backward otherwise prepares from k and v.  The forward builds the RoPE
-factors of three rows in four by a recurrence and the backward's own preparation reads them
+factors of two rows in three by a recurrence and the backward's own preparation reads them
 from the tables, so a K' element can differ in its last float16 bit: the prepared backward
 must match fib_attn_bwd to within that rounding (relative L2 <= 2e-3 for dQ, dK, dV and
 dalpha), be deterministic, and match the float64 oracle with the parity tests' bounds,
