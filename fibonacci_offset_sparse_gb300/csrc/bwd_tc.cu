@@ -120,8 +120,10 @@ __device__ __forceinline__ void store_plain(__nv_bfloat16* row, const float (&ac
 // One thread per (row, quarter u), frequencies m = 8u .. 8u+7 (chunks u and u+4 of a row):
 // the four f16 arrays, and Delta by a quad reduction.  Without KV (K' and V' prepared by the
 // layer's forward and handed over), only Q's, dO' and Delta.
+constexpr int kBPrepThreads = 128;  // four threads a row (128: measured best of 64-512)
+
 template <bool KV>
-__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ q,
+__global__ void __launch_bounds__(kBPrepThreads) bwd_prep_kernel(const __nv_bfloat16* __restrict__ q,
                                                        const __nv_bfloat16* __restrict__ k,
                                                        const __nv_bfloat16* __restrict__ v,
                                                        const __nv_bfloat16* __restrict__ o,
@@ -134,7 +136,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   // The dependent dQ grid may launch at once (its CTAs take the SMs as this grid drains);
   // it waits for the whole of this grid before it reads what this grid writes.
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  const long long gid = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  const long long gid = static_cast<long long>(blockIdx.x) * kBPrepThreads + threadIdx.x;
   const long long row = gid >> 2;
   const unsigned active = __ballot_sync(0xffffffffu, row < rows);  // whole quads
   if (row >= rows) return;
@@ -839,14 +841,14 @@ cudaError_t launch_half(const LayerTable& t, long long off, long long n, int N, 
   a.status = status;
   a.wait_ns = wait_ns;
   const long long blocks = static_cast<long long>(a.tiles) * n;
-  const long long prep_blocks = (rows * 4 + 255) / 256;
+  const long long prep_blocks = (rows * 4 + kBPrepThreads - 1) / kBPrepThreads;
   if (blocks > 0x7fffffffLL || prep_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (kv_k == nullptr)
-    bwd_prep_kernel<true><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
+    bwd_prep_kernel<true><<<static_cast<unsigned>(prep_blocks), kBPrepThreads, 0, stream>>>(
         bf(q), bf(k), bf(v), bf(o), bf(dO), const_cast<__half*>(a.qs), const_cast<__half*>(a.kp),
         const_cast<__half*>(a.vp), const_cast<__half*>(a.dos), delta, lo_tab, hi_tab, N, rows, kLog2e / 8.0f, status);
   else
-    bwd_prep_kernel<false><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
+    bwd_prep_kernel<false><<<static_cast<unsigned>(prep_blocks), kBPrepThreads, 0, stream>>>(
         bf(q), nullptr, nullptr, bf(o), bf(dO), const_cast<__half*>(a.qs), nullptr, nullptr,
         const_cast<__half*>(a.dos), delta, lo_tab, hi_tab, N, rows, kLog2e / 8.0f, status);
   cudaError_t e;
