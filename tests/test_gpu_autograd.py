@@ -21,9 +21,11 @@ def _lib():
     return fa.lib()
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_autograd_is_the_library_forward_and_backward(dtype):
-    B, H, N, W, L = 2, 2, 300, 8, 3
+@pytest.mark.parametrize("dtype,W", [("f32", 8), ("bf16", 8), ("bf16", 20)])
+def test_autograd_is_the_library_forward_and_backward(dtype, W):
+    """The Function's outputs and gradients are the library calls' bit for bit: from the kept
+    K'/V' workspace where the forward prepares one (bf16, W <= 16), else from k and v."""
+    B, H, N, L = 2, 2, 300, 3
     plan = fa.fib_attn_plan_create(fa.FIB_BASE_FIBONACCI, [1.0] * L, W, N, fa.FIB_MODE_INTERP)
     alpha = torch.tensor([0.9, 1.2345, 1.1], dtype=torch.float32, device="cuda", requires_grad=True)
     q, k, v = (t.cuda().requires_grad_(True) for t in inputs.qkv(B, H, N, 64, 300, 1, dtype))

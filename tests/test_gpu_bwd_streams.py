@@ -95,11 +95,20 @@ def test_results_are_ordered_on_the_callers_stream():
     plan.close()
 
 
-def test_graph_replay_equals_the_eager_backward():
-    """The backward captured in a CUDA graph on the caller's stream (the side stream joins the
-    capture through the fork event) and replayed twice gives the eager result bit for bit."""
+@pytest.mark.parametrize("entry", ["bwd", "bwd_prepared"])
+def test_graph_replay_equals_the_eager_backward(entry):
+    """The backward (from k and v, or from the forward's prepared K'/V') captured in a CUDA
+    graph on the caller's stream (the side stream joins the capture through the fork event)
+    and replayed twice gives the eager result bit for bit."""
     plan, (q, k, v, o, lse, dO), adev = _case()
-    ref = fa.fib_attn_bwd(plan, 0, q, k, v, o, lse, dO, alpha_dev=adev)
+    kv = torch.empty(fa.fib_attn_fwd_workspace_size(plan, *q.shape[:3], q.dtype), dtype=torch.uint8, device="cuda")
+    fa.fib_attn_fwd_prepare_kv(plan, k, v, workspace=kv)
+
+    def run(*out, **kw):
+        if entry == "bwd":
+            return fa.fib_attn_bwd(plan, 0, q, k, v, o, lse, dO, *out, alpha_dev=adev, **kw)
+        return fa.fib_attn_bwd_prepared(plan, 0, q, kv, o, lse, dO, *out, alpha_dev=adev, **kw)
+    ref = run()
     torch.cuda.synchronize()
     outs = [torch.empty_like(q) for _ in range(3)]
     da = torch.empty(1, dtype=torch.float32, device="cuda")
@@ -107,11 +116,11 @@ def test_graph_replay_equals_the_eager_backward():
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):  # one eager call on the capture stream first (as torch advises)
-        fa.fib_attn_bwd(plan, 0, q, k, v, o, lse, dO, *outs, dalpha=da, alpha_dev=adev, workspace=ws)
+        run(*outs, dalpha=da, workspace=ws)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        fa.fib_attn_bwd(plan, 0, q, k, v, o, lse, dO, *outs, dalpha=da, alpha_dev=adev, workspace=ws)
+        run(*outs, dalpha=da, workspace=ws)
     for _ in range(2):
         for x in outs + [da]:
             x.fill_(float("nan"))
