@@ -248,9 +248,9 @@ int fib_attn_bwd(fib_attn_plan_t p, int layer, int B, int H, int N, int dtype,
  * only Q', dO' and Delta.  Results equal those of fib_attn_bwd on the same inputs up to the
  * float16 rounding of K' (the forward builds the RoPE factors of two rows in three by a
  * recurrence, the backward's own preparation reads them from the tables, so a K' element
- * can differ in its last bit); both are deterministic.  kv_prepared: that workspace,
- * kv_bytes >= fib_attn_fwd_workspace_size(p, B, H, N,
- * dtype), 256-byte aligned, read only.  Everything else as fib_attn_bwd, plus
+ * can differ in its last bit); both are deterministic.  kv_prepared: that workspace, of
+ * kv_bytes >= fib_attn_fwd_workspace_size(p, B, H, N, dtype), 256-byte aligned, read only.
+ * Everything else as fib_attn_bwd, plus
  * FIB_ERR_UNSUPPORTED where the forward has no prepared rows (float32, or W > 16: call
  * fib_attn_bwd there) and FIB_ERR_INVALID_ARG for a short or misaligned kv_prepared or one
  * that is the backward workspace or an output.                                          */
