@@ -130,3 +130,29 @@ def test_graph_replay_equals_the_eager_backward(entry):
             assert torch.equal(x, r)
     assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
     plan.close()
+
+
+def test_two_plans_run_their_backwards_concurrently():
+    """Two plans (each with its own side stream) on two caller streams at once: every result
+    equals the same call made alone, bit for bit."""
+    cases = []
+    for i, (alpha, mode) in enumerate(((0.9871, "interp"), (1.3, "mask"))):
+        plan = _plan(alpha, 12, 640, mode)
+        q, k, v = (t.cuda() for t in inputs.qkv(2, 2, 640, 64, 770 + i, 0, "bf16"))
+        dO = inputs.upstream_grad(2, 2, 640, 64, 770 + i, 0, "bf16").cuda()
+        o, lse = fa.fib_attn_fwd(plan, 0, q, k, v)
+        ref = fa.fib_attn_bwd(plan, 0, q, k, v, o, lse, dO)
+        cases.append((plan, (q, k, v, o, lse, dO), ref))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    got = []
+    for s, (plan, args, _) in zip(streams, cases):
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            got.append(fa.fib_attn_bwd(plan, 0, *args))
+    torch.cuda.synchronize()
+    for g, (plan, _, ref) in zip(got, cases):
+        for x, r in zip(g, ref):
+            assert torch.equal(x, r)
+        assert fa.fib_attn_last_device_status(plan) == fa.FIB_OK
+        plan.close()
